@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Throughput of the fused SSIM loss: fp32 forward + backward, megapixels/s.
+
+Workload: the 1080p splatting-render pair, 1 x 3 x 1080 x 1920 float32,
+padding "valid", gradient for img1 only (TriSSIM README, "Performance": 1080p,
+fp32, valid, forward + backward).  A step is one ssim_fwd (training mode, the
+gradient fields saved) plus one ssim_bwd, back to back on one stream, through
+the C ABI.  MP = N*H*W / 1e6 input pixels per step (channels not counted).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  With N > 1 (torchrun, one process per GPU) every rank
+processes its own image -- the batch is sharded, there is no data exchange --
+and the time is the maximum over ranks ("scaling": "weak").
+
+--impl reference times the CPU oracle (test infrastructure: the plain
+double-precision statement of the loss) on the host cores, each step a bounded
+band of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "splat1080_valid"
+METRIC = "fp32 SSIM fwd+bwd megapixels/s at 1080p valid; % of HBM roofline"
+UNIT = "MP/s"
+NOMINAL_HBM_GBS = 8000.0
+FLUSH_BYTES = 256 << 20
+KERNEL_NAME = "ssim2d_stream_kernel<true,false>"
+PROFILE = os.path.join(ROOT, "profiles", "ssim2d_grad_splat1080_valid.md")
+
+# Algorithmic float32 operations of the gradient-mode kernel per input pixel
+# (fused forward statistics, SSIM derivatives, adjoint and chain rule), counting
+# an FMA as 2 flops; derivation in DESIGN.md ("Roofline of each kernel").
+GRAD_FMA_PER_PIXEL = 44 + 44 + 33 + 33  # row + column passes of 4 statistics, of 3 adjoint maps
+GRAD_OTHER_PER_PIXEL = 5 + 30 + 3       # shifted products, SSIM and derivatives, chain rule
+GRAD_FLOPS_PER_PIXEL = 2 * GRAD_FMA_PER_PIXEL + GRAD_OTHER_PER_PIXEL
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra timed variants")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms meanwhile."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in loaded),
+                "power_w_max": max(r[2] for r in loaded),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def oracle_band(n_rows: int):
+    """(x, y, dl) for the first n_rows rows of the workload pair (a bounded sample)."""
+    from workloads import dl_vector, make_inputs
+
+    x, y = make_inputs(WORKLOAD)
+    n_rows = max(11, min(n_rows, x.shape[2]))
+    return (x[:, :, :n_rows].copy(), y[:, :, :n_rows].copy(), dl_vector(WORKLOAD))
+
+
+def time_oracle_step(oracle, x, y, dl):
+    t0 = time.perf_counter()
+    oracle.ssim2d(x, y, "valid")
+    oracle.ssim2d_grad(x, y, dl, "valid", want_grad2=False)
+    return time.perf_counter() - t0
+
+
+def size_oracle_band(oracle, target_s: float):
+    """Rows of the 1080p pair whose oracle step takes about target_s seconds."""
+    rows = 32
+    x, y, dl = oracle_band(rows)
+    t = time_oracle_step(oracle, x, y, dl)
+    while t < target_s / 2 and rows < 1080:
+        rows = min(1080, int(rows * min(8.0, max(2.0, target_s / max(t, 1e-3)))))
+        x, y, dl = oracle_band(rows)
+        t = time_oracle_step(oracle, x, y, dl)
+    return rows, (x, y, dl), t
+
+
+def cpu_baseline(target_s: float = 4.0):
+    import oracle
+
+    oracle.build()
+    rows, (x, y, dl), _ = size_oracle_band(oracle, target_s)
+    times = [time_oracle_step(oracle, x, y, dl) for _ in range(3)]
+    t = statistics.median(times)
+    mp = x.shape[0] * x.shape[2] * x.shape[3] / 1e6
+    return {"value": mp / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows} of the 1x3x1080x1920 pair (valid), mean + grad_img1, "
+                      f"median of 3 ({t:.2f} s each)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    budget = 150.0  # seconds for the whole run
+    per_step = max(0.5, min(5.0, budget / max(1, args.steps + args.warmup)))
+    rows, (x, y, dl), _ = size_oracle_band(oracle, per_step)
+    for _ in range(args.warmup):
+        time_oracle_step(oracle, x, y, dl)
+    times = [time_oracle_step(oracle, x, y, dl) for _ in range(args.steps)]
+    mp = x.shape[0] * x.shape[2] * x.shape[3] / 1e6
+    total = sum(times)
+    value = mp * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shape": [1, 3, 1080, 1920], "padding": "valid",
+                   "grads": "img1", "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"rows 0..{rows} of the 1x3x1080x1920 pair per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "differentiable_image_quality_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the gradient kernel from the committed ncu
+    summary, if it was taken from the current kernel sources; else None."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_digest():
+        return None
+    return float(m.group(1))
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import differentiable_image_quality_gb300 as pkg
+    from workloads import WORKLOADS, dl_vector, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg._abi.load()
+    wl = WORKLOADS[WORKLOAD]
+    x, y = make_inputs(WORKLOAD)
+    dl = dl_vector(WORKLOAD)
+    N, C, H, W = x.shape
+    mp = N * H * W / 1e6
+
+    tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+    tdl = torch.from_numpy(dl).to(dev)
+    mean = torch.empty(N, device=dev)
+    saved = torch.empty(pkg.saved_bytes(x.shape, False) // 4, device=dev)
+    g1 = torch.empty_like(tx)
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_saved():
+        pkg.ssim_fwd(tx, ty, wl.padding, mean, saved=saved, want_grad2=False)
+        pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1, saved=saved)
+
+    def timed(fn_a, fn_b, steps, warmup):
+        """Per-step device times of fn_a then fn_b, L2 flushed before each step."""
+        for _ in range(warmup):
+            flush.zero_()
+            fn_a()
+            if fn_b:
+                fn_b()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            fn_a()
+            e[1].record(stream)
+            if fn_b:
+                fn_b()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ta = [e[0].elapsed_time(e[1]) for e in ev]
+        tb = [e[1].elapsed_time(e[2]) for e in ev]
+        return ta, tb
+
+    def fwd_train():
+        pkg.ssim_fwd(tx, ty, wl.padding, mean, saved=saved, want_grad2=False)
+
+    def bwd_saved():
+        pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1, saved=saved)
+
+    with ClockSampler(local) as clocks:
+        ta, tb = timed(fwd_train, bwd_saved, args.steps, max(3, args.warmup))
+    clk = clocks.summary()
+
+    step_ms = [a + b for a, b in zip(ta, tb)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * mp * args.steps / (total_ms / 1e3)
+    fwd_ms = statistics.mean(ta)
+    bwd_ms = statistics.mean(tb)
+
+    # ---- end to end through the public API with host buffers (pinned)
+    hx = torch.from_numpy(x).pin_memory()
+    hy = torch.from_numpy(y).pin_memory()
+    hg = torch.empty(x.shape, dtype=torch.float32).pin_memory()
+    hm = torch.empty(N, dtype=torch.float32).pin_memory()
+    dx, dy = torch.empty_like(tx), torch.empty_like(ty)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dy.copy_(hy, non_blocking=True)
+        pkg.ssim_fwd(dx, dy, wl.padding, mean, saved=saved, want_grad2=False)
+        pkg.ssim_bwd(tdl, dx, dy, wl.padding, g1, saved=saved)
+        hg.copy_(g1, non_blocking=True)
+        hm.copy_(mean, non_blocking=True)
+
+    te, _ = timed(e2e_step, None, args.steps, max(3, args.warmup))
+    e2e_ms = sum(te)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * mp * args.steps / (e2e_ms / 1e3)
+
+    extras = {}
+    if not args.no_extras:
+        # recompute backward (no saved fields) and the inference forward
+        def fwd_infer():
+            pkg.ssim_fwd(tx, ty, wl.padding, mean)
+
+        def bwd_recompute():
+            pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1)
+
+        ra, rb = timed(fwd_infer, bwd_recompute, args.steps, 3)
+        extras = {
+            "fwd_train_mps": mp / (fwd_ms / 1e3),
+            "bwd_saved_mps": mp / (bwd_ms / 1e3),
+            "fwd_infer_mps": mp / (statistics.mean(ra) / 1e3),
+            "bwd_recompute_mps": mp / (statistics.mean(rb) / 1e3),
+            "recompute_path_fwd_bwd_mps": mp / ((statistics.mean(ra) + statistics.mean(rb)) / 1e3),
+        }
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_kind = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sm_count = props.multi_processor_count
+    sm_max = float(clk.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0))
+    alu_peak_tflops = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
+    grad_flops = GRAD_FLOPS_PER_PIXEL * N * C * H * W
+    achieved_tflops = grad_flops / (fwd_ms / 1e3) / 1e12
+    min_bytes = (2 * N * C * H * W + 2 * N * C * H * W + N * C * H * W) * 4  # fwd 2 reads; bwd 2 reads + 1 write
+    step_s = statistics.mean(step_ms) / 1e3
+    hbm_gbs = min_bytes / step_s / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shape": [N, C, H, W], "padding": wl.padding,
+                   "grads": "img1", "path": "saved gradient fields (training forward) + scaling backward",
+                   "l2": "flushed before every step (256 MiB write outside the timed events)",
+                   "timing": "CUDA events per step on the launching stream; value = K steps / sum"},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"kernel": KERNEL_NAME, "bound": "alu", "achieved": achieved_tflops,
+                     "peak": alu_peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved_tflops / alu_peak_tflops,
+                     "traffic": profiled_traffic(),
+                     "peak_basis": f"{sm_count} SMs x 128 fp32 lanes x 2 flops x {sm_max:.0f} MHz",
+                     "flops_per_pixel": GRAD_FLOPS_PER_PIXEL},
+        "hbm_roofline": {"min_bytes_per_step": min_bytes, "achieved_gbs": hbm_gbs,
+                         "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
+                         "frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
+                         "measured_peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": 2 * N * C * H * W * 4,
+                "d2h_bytes_per_step": N * C * H * W * 4 + N * 4},
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        **extras,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,79 @@
+"""ctypes view of the C ABI declared in include/gbssim.h.
+
+Only argument marshalling happens here: tensors become device pointers, the
+current CUDA stream becomes the `stream` argument, and a negative status
+becomes a Python exception.  Every step of the computation runs in libgbssim.so.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+VALID, SAME = 0, 1
+PADDING = {"valid": VALID, "same": SAME}
+
+_lock = threading.Lock()
+_lib = None
+
+# names the header declares, with (restype, argtypes)
+_vp, _sz, _i, _fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+SIGNATURES = {
+    "gbssim_abi_version": (_i, []),
+    "gbssim_strerror": (ctypes.c_char_p, [_i]),
+    "gbssim_window": (None, [ctypes.POINTER(ctypes.c_float)]),
+    "gbssim_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "gbssim_saved_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "ssim_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),
+    "ssim_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp]),
+    "gbssim3d_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "gbssim3d_saved_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "ssim3d_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),
+    "ssim3d_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp]),
+}
+# exported beyond the header: the planner's tuning hook
+EXTRA = {"gbssim_tune_seg_rows": (None, [_i])}
+
+
+class GbssimError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed: status {status}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libgbssim.so.  Raises when it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            if build_if_missing:
+                _build.build()
+            else:
+                raise RuntimeError(
+                    "libgbssim.so is not built: run `python -c \"import __graft_entry__ as g; "
+                    "g.build()\"` or differentiable_image_quality_gb300._build.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in {**SIGNATURES, **EXTRA}.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def check(fn: str, status: int) -> None:
+    if status != 0:
+        msg = load().gbssim_strerror(status).decode()
+        raise GbssimError(fn, status, msg)
+
+
+def ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()

@@ -1,0 +1,168 @@
+// Shared device helpers of the SSIM kernels (sm_103a).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gbssim {
+
+// The eleven taps of the window: float32 roundings of exp(-(k-5)^2 / (2 * 1.5^2)),
+// k = 0..10, divided by their sum (fused-ssim README introduction: a fixed 11x11
+// Gaussian window "as per the original SSIM paper"; sigma 1.5).  Symmetric:
+// w(k) = w(10 - k), six distinct values.
+__host__ __device__ constexpr float tap(int k)
+{
+    return (k == 0 || k == 10)  ? 1.028380124e-03f
+           : (k == 1 || k == 9) ? 7.598758209e-03f
+           : (k == 2 || k == 8) ? 3.600077331e-02f
+           : (k == 3 || k == 7) ? 1.093606874e-01f
+           : (k == 4 || k == 6) ? 2.130055428e-01f
+                                : 2.660117149e-01f;
+}
+
+constexpr int kTaps = 11;
+constexpr int kRadius = 5;
+
+// Stabilising constants for data range 1 (fused-ssim README, "Constraints").
+constexpr float kC1 = 1.0e-4f;  // (0.01 * 1)^2
+constexpr float kC2 = 9.0e-4f;  // (0.03 * 1)^2
+
+// Every value enters the products as (v - kShift), the image being extended
+// by zeros, i.e. the shifted image by -kShift.  The variances and covariance are
+// invariant under a common shift of the window's values when the window's
+// weights sum to one, which they do once the zero extension is counted; the
+// shift only reduces float32 cancellation in E[x^2] - mu^2 (values in [0, 1]).
+constexpr float kShift = 0.5f;
+
+// ------------------------------------------------------------ cp.async helpers
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool in_bounds)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int src_bytes = in_bounds ? 4 : 0;  // 0: write zeros, read nothing
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int Pending>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(Pending) : "memory");
+}
+
+// ------------------------------------------------------------ SSIM at a pixel
+
+// Statistics of one window in shifted form: m1 = E[x'], m2 = E[y'],
+// es = E[x'^2] + E[y'^2], e12 = E[x'y'], with x' = x - kShift, y' = y - kShift.
+struct Moments {
+    float m1, m2, es, e12;
+};
+
+// Upstream gradients of S with respect to the shifted moments (m1, m2, es, e12).
+// Because sigma11 and sigma22 enter S only as their sum, dS/dE[x'^2] and
+// dS/dE[y'^2] are one value, g_e.
+struct MomentGrads {
+    float g_m1, g_m2, g_e, g_e12;
+};
+
+// S = A1 A2 / (B1 B2) with
+//   mu = m + kShift, sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2,
+//   A1 = 2 mu1 mu2 + C1, A2 = 2 sigma12 + C2, B1 = mu1^2 + mu2^2 + C1,
+//   B2 = sigma_sum + C2.
+__device__ __forceinline__ float ssim_value(const Moments &m)
+{
+    const float mu1 = m.m1 + kShift, mu2 = m.m2 + kShift;
+    const float ss = m.es - m.m1 * m.m1 - m.m2 * m.m2;
+    const float s12 = m.e12 - m.m1 * m.m2;
+    const float A1 = 2.0f * mu1 * mu2 + kC1;
+    const float A2 = 2.0f * s12 + kC2;
+    const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
+    const float B2 = ss + kC2;
+    return __fdividef(A1 * A2, B1 * B2);
+}
+
+// S and its derivatives with respect to the shifted moments.
+//   dS/dsigma_sum = -S / B2,  dS/dsigma12 = 2 A1 / (B1 B2),
+//   dS/dmu1 (sigmas fixed) = 2 (mu2 A2 - mu1 S B2) / (B1 B2),
+// and through sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2:
+//   dS/dm1 = dS/dmu1 - 2 m1 dS/dsigma_sum - m2 dS/dsigma12   (m2 likewise).
+__device__ __forceinline__ float ssim_and_grads(const Moments &m, MomentGrads &g)
+{
+    const float mu1 = m.m1 + kShift, mu2 = m.m2 + kShift;
+    const float ss = m.es - m.m1 * m.m1 - m.m2 * m.m2;
+    const float s12 = m.e12 - m.m1 * m.m2;
+    const float A1 = 2.0f * mu1 * mu2 + kC1;
+    const float A2 = 2.0f * s12 + kC2;
+    const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
+    const float B2 = ss + kC2;
+    const float inv = __fdividef(1.0f, B1 * B2);
+    const float S = A1 * A2 * inv;
+    const float d_ss = -S * B1 * inv;      // -S / B2
+    const float d_s12 = 2.0f * A1 * inv;
+    const float SB2 = S * B2;
+    const float d_mu1 = 2.0f * inv * (mu2 * A2 - mu1 * SB2);
+    const float d_mu2 = 2.0f * inv * (mu1 * A2 - mu2 * SB2);
+    g.g_m1 = d_mu1 - 2.0f * m.m1 * d_ss - m.m2 * d_s12;
+    g.g_m2 = d_mu2 - 2.0f * m.m2 * d_ss - m.m1 * d_s12;
+    g.g_e = d_ss;
+    g.g_e12 = d_s12;
+    return S;
+}
+
+// ------------------------------------------------------------ block reduction
+
+// Sum of one float per thread over a block of NT threads (NT a multiple of 32),
+// in double; returns the total in thread 0.  Fixed order: deterministic.
+template <int NT>
+__device__ __forceinline__ double block_sum(float v, double *scratch /* NT/32 doubles */)
+{
+    double d = static_cast<double>(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_down_sync(0xffffffffu, d, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) scratch[warp] = d;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) t += scratch[w];
+    }
+    return t;
+}
+
+// Grid-wide finish of the per-image means.  Every block calls this once, with
+// its partial sum already written to partials[blockIdx.x] by thread 0.  The
+// last block to arrive sums each image's partials in block order (double) and
+// writes mean[n] = sum / count, then resets the counter to zero for the next
+// call.  blocks_per_image consecutive blocks belong to one image.
+template <int NT>
+__device__ __forceinline__ void finish_means(double *partials, unsigned *counter, float *mean,
+                                             int images, int blocks_per_image, double count)
+{
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned total = gridDim.x;
+        const unsigned ticket = atomicAdd(counter, 1u);
+        last = (ticket == total - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int n = threadIdx.x; n < images; n += NT) {
+        const double *p = partials + static_cast<size_t>(n) * blocks_per_image;
+        double s = 0.0;
+        for (int b = 0; b < blocks_per_image; ++b) s += __ldcg(p + b);
+        mean[n] = static_cast<float>(s / count);
+    }
+    if (threadIdx.x == 0) *counter = 0u;
+}
+
+}  // namespace gbssim

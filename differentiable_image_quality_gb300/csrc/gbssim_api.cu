@@ -1,0 +1,317 @@
+// The C ABI (include/gbssim.h): argument checks, launch planning, dispatch.
+// Host code only; every step of the computation runs in the kernels.
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/gbssim.h"
+#include "common.cuh"
+#include "ssim2d.cuh"
+#include "ssim3d.cuh"
+
+namespace {
+
+using namespace gbssim;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinSegRows = 22;    // shortest row segment the planner uses
+constexpr size_t kCounterBytes = 256;  // completion counter, then the partial sums
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+int g_seg_rows_override = 0;  // tuning: 0 = planner's choice
+
+int cuda_fail(cudaError_t e)
+{
+    (void)cudaGetLastError();  // clear a sticky launch error so the next call starts clean
+    return e == cudaSuccess ? GBSSIM_OK : GBSSIM_ECUDA;
+}
+
+// Per-device launch facts, filled once per device with that device current.
+int device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cuda_fail(cudaErrorInvalidDevice);
+        const bool grad[3] = {false, true, true}, g2[3] = {false, false, true};
+        for (int i = 0; i < 3; ++i) {
+            const void *k = ssim2d_kernel_ptr(grad[i], g2[i]);
+            const size_t smem = ssim2d_smem_bytes(grad[i]);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(smem));
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ2d[i], k, kThreads2d, smem);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (d.occ2d[i] < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+        }
+        int rc = ssim3d_prepare_device();
+        if (rc != GBSSIM_OK) return rc;
+        d.ready = true;
+    }
+    *out = &d;
+    return GBSSIM_OK;
+}
+
+int check_in(const void *p)
+{
+    if (!p) return GBSSIM_EINVAL;
+    if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return GBSSIM_EALIGN;
+    return GBSSIM_OK;
+}
+
+int check_opt(const void *p) { return p ? check_in(p) : GBSSIM_OK; }
+
+int extent_ok(int n, int padding)
+{
+    if (padding == GBSSIM_VALID) return n >= kTaps;
+    if (padding == GBSSIM_SAME_ZERO) return n >= 1;
+    return 0;
+}
+
+int out_extent(int n, int padding) { return padding == GBSSIM_VALID ? n - (kTaps - 1) : n; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Launch plan of the 2D streaming kernel: column strips x row segments x planes.
+struct Plan2d {
+    int strips = 0, segs = 0, seg_rows = 0;
+    long long blocks = 0;
+};
+
+// Pick the row segmentation.  Time is modelled per SM: the busiest SM holds
+// ceil(blocks / SMs) blocks of `steps` row steps each, and an SM with fewer than
+// two resident blocks runs at a proportionally lower rate.
+Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, bool grad, int sm_count, int occ)
+{
+    Plan2d p;
+    const int cols = grad ? W : Wo;
+    const int rows = grad ? H : Ho;
+    const int halo = grad ? 20 : 10;
+    p.strips = int(ceil_div(cols, grad ? ssim2d_grad_cols() : ssim2d_stat_cols()));
+    const long long cols_planes = (long long)p.strips * planes;
+    const int sat = occ < 2 ? occ : 2;
+    const int max_segs = int(ceil_div(rows, kMinSegRows));
+    double best = -1.0;
+    long long best_work = 0;
+    for (int s = 1; s <= max_segs; ++s) {
+        int sr = int(ceil_div(rows, s));
+        if (g_seg_rows_override > 0) sr = g_seg_rows_override < rows ? g_seg_rows_override : rows;
+        const int segs = int(ceil_div(rows, sr));
+        const long long blocks = cols_planes * segs;
+        const long long steps = ceil_div(sr + halo, kTaps);
+        const long long per_sm = ceil_div(blocks, sm_count);
+        const double eff = double(per_sm < sat ? per_sm : sat) / sat;
+        const double cost = double(per_sm * steps) / eff;
+        const long long work = blocks * steps;
+        if (best < 0 || cost < best - 1e-9 || (cost <= best + 1e-9 && work < best_work)) {
+            best = cost;
+            best_work = work;
+            p.segs = segs;
+            p.seg_rows = sr;
+            p.blocks = blocks;
+        }
+        if (g_seg_rows_override > 0) break;
+    }
+    return p;
+}
+
+// Upper bound of blocks over every plan (segments never shorter than kMinSegRows).
+long long max_blocks2d(long long planes, int H, int W, int Ho, int Wo)
+{
+    const long long g = ceil_div(W, ssim2d_grad_cols()) * ceil_div(H, kMinSegRows);
+    const long long f = ceil_div(Wo, ssim2d_stat_cols()) * ceil_div(Ho, kMinSegRows);
+    return planes * (g > f ? g : f);
+}
+
+bool shape2d_ok(int N, int C, int H, int W, int padding)
+{
+    if (N < 1 || C < 1) return false;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return false;
+    if (!extent_ok(H, padding) || !extent_ok(W, padding)) return false;
+    if ((long long)N * C > INT_MAX) return false;
+    if (H > (1 << 28) || W > (1 << 28)) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gbssim_abi_version(void) { return GBSSIM_ABI_VERSION; }
+
+const char *gbssim_strerror(int status)
+{
+    switch (status) {
+    case GBSSIM_OK: return "ok";
+    case GBSSIM_EINVAL: return "invalid argument (null pointer, bad padding or overlapping buffers)";
+    case GBSSIM_ESHAPE: return "invalid shape (N or C < 1, an extent below the window, or too large)";
+    case GBSSIM_EALIGN: return "misaligned pointer (float32 buffers need 4-byte alignment)";
+    case GBSSIM_EWORKSPACE: return "workspace or saved buffer missing or too small";
+    case GBSSIM_ECUDA: return "a CUDA runtime call or kernel launch failed";
+    default: return "unknown status";
+    }
+}
+
+void gbssim_window(float w[11])
+{
+    if (!w) return;
+    for (int k = 0; k < kTaps; ++k) w[k] = tap(k);
+}
+
+// Tuning hook for benchmarks: force the row-segment length of the 2D planner
+// (0 restores the planner; lengths below the planner's minimum are raised to
+// it).  Results do not depend on it.
+void gbssim_tune_seg_rows(int rows)
+{
+    g_seg_rows_override = rows > 0 ? (rows < kMinSegRows ? kMinSegRows : rows) : 0;
+}
+
+size_t gbssim_workspace_bytes(int N, int C, int H, int W, int padding)
+{
+    if (!shape2d_ok(N, C, H, W, padding)) return 0;
+    const long long b = max_blocks2d((long long)N * C, H, W, out_extent(H, padding),
+                                     out_extent(W, padding));
+    return kCounterBytes + size_t(b) * sizeof(double);
+}
+
+size_t gbssim_saved_bytes(int N, int C, int H, int W, int want_grad2)
+{
+    if (N < 1 || C < 1 || H < 1 || W < 1) return 0;
+    const size_t field = size_t(N) * C * H * W * sizeof(float);
+    return want_grad2 ? 2 * field : field;
+}
+
+int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+             float *out_mean, float *out_map_or_null, float *saved_or_null, size_t saved_bytes,
+             int want_grad2, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_mean)) ||
+        (rc = check_opt(out_map_or_null)) || (rc = check_opt(saved_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape2d_ok(N, C, H, W, padding)) return GBSSIM_ESHAPE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return GBSSIM_EWORKSPACE;
+    const bool grad = saved_or_null != nullptr;
+    const size_t img_bytes = size_t(N) * C * H * W * sizeof(float);
+    if (grad && saved_bytes < gbssim_saved_bytes(N, C, H, W, want_grad2))
+        return GBSSIM_EWORKSPACE;
+    const int Ho = out_extent(H, padding), Wo = out_extent(W, padding);
+    const size_t map_bytes = size_t(N) * C * Ho * Wo * sizeof(float);
+    if (grad && (overlaps(saved_or_null, saved_bytes, img1, img_bytes) ||
+                 overlaps(saved_or_null, saved_bytes, img2, img_bytes) ||
+                 overlaps(saved_or_null, saved_bytes, out_map_or_null, map_bytes)))
+        return GBSSIM_EINVAL;
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    const int occ = d->occ2d[grad ? (want_grad2 ? 2 : 1) : 0];
+    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, grad, d->sm_count, occ);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
+        return GBSSIM_EWORKSPACE;
+
+    Ssim2dArgs a{};
+    a.x = img1; a.y = img2;
+    a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
+    a.off = padding == GBSSIM_VALID ? 0 : kRadius;
+    a.C = C;
+    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    a.out1 = grad ? saved_or_null : nullptr;
+    a.out2 = (grad && want_grad2) ? saved_or_null + size_t(N) * C * H * W : nullptr;
+    a.dL = nullptr;
+    a.inv_count = float(1.0 / (double(C) * double(Ho) * double(Wo)));
+    a.map = out_map_or_null;
+    a.counter = static_cast<unsigned *>(workspace);
+    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
+    a.mean = out_mean;
+    a.images = N;
+    a.blocks_per_image = int(p.blocks / N);
+    a.count = double(C) * double(Ho) * double(Wo);
+    return cuda_fail(ssim2d_launch(a, grad, grad && want_grad2, int(p.blocks),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int H, int W,
+             int padding, const float *saved_or_null, size_t saved_bytes, float *grad_img1,
+             float *grad_img2_or_null, void *stream)
+{
+    int rc;
+    if ((rc = check_in(dL)) || (rc = check_in(img1)) || (rc = check_in(img2)) ||
+        (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)) ||
+        (rc = check_opt(saved_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape2d_ok(N, C, H, W, padding)) return GBSSIM_ESHAPE;
+    const size_t total = size_t(N) * C * H * W;
+    const size_t img_bytes = total * sizeof(float);
+    const bool g2 = grad_img2_or_null != nullptr;
+    // gradients may not overlap the images, dL or each other
+    if (overlaps(grad_img1, img_bytes, img1, img_bytes) ||
+        overlaps(grad_img1, img_bytes, img2, img_bytes) ||
+        overlaps(grad_img1, img_bytes, dL, size_t(N) * sizeof(float)) ||
+        (g2 && (overlaps(grad_img2_or_null, img_bytes, img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, img2, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, dL, size_t(N) * sizeof(float)) ||
+                overlaps(grad_img2_or_null, img_bytes, grad_img1, img_bytes))))
+        return GBSSIM_EINVAL;
+
+    const float *f1 = saved_or_null, *f2 = (saved_or_null && g2) ? saved_or_null + total : nullptr;
+    if (saved_or_null) {
+        if (saved_bytes < gbssim_saved_bytes(N, C, H, W, g2)) return GBSSIM_EWORKSPACE;
+        // a gradient may be the saved field itself (scaled in place), but not a shifted overlap
+        if ((overlaps(grad_img1, img_bytes, saved_or_null, saved_bytes) && grad_img1 != f1) ||
+            (g2 && overlaps(grad_img2_or_null, img_bytes, saved_or_null, saved_bytes) &&
+             grad_img2_or_null != f2))
+            return GBSSIM_EINVAL;
+    }
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    const int Ho = out_extent(H, padding), Wo = out_extent(W, padding);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (saved_or_null)
+        return cuda_fail(scale_fields_launch(f1, f2, grad_img1, grad_img2_or_null, dL, 1.0f,
+                                             size_t(C) * H * W, total, d->sm_count, s));
+    const int occ = d->occ2d[g2 ? 2 : 1];
+    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, true, d->sm_count, occ);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    Ssim2dArgs a{};
+    a.x = img1; a.y = img2;
+    a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
+    a.off = padding == GBSSIM_VALID ? 0 : kRadius;
+    a.C = C;
+    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    a.out1 = grad_img1;
+    a.out2 = grad_img2_or_null;
+    a.dL = dL;
+    a.inv_count = float(1.0 / (double(C) * double(Ho) * double(Wo)));
+    a.map = nullptr;
+    a.partials = nullptr;
+    a.counter = nullptr;
+    a.mean = nullptr;
+    a.images = N;
+    a.blocks_per_image = int(p.blocks / N);
+    a.count = double(C) * double(Ho) * double(Wo);
+    return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), s));
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+/*
+ * gbssim.h -- C ABI of a fused, differentiable SSIM loss for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (per image n, channel c, output pixel p of the domain Omega):
+ *   mu1, mu2, E[x^2], E[y^2], E[xy] under an 11x11 Gaussian window (sigma 1.5,
+ *   weights normalised to sum to one) -- the five blurred quantities of the
+ *   TriSSIM README, "How it works", with the fixed 11x11 window of the fused-ssim
+ *   README introduction;
+ *   S(p) = (2 mu1 mu2 + C1)(2 sigma12 + C2) / ((mu1^2 + mu2^2 + C1)(sigma11 + sigma22 + C2)),
+ *   C1 = 0.01^2, C2 = 0.03^2 (images in [0, 1]: fused-ssim README, "Constraints");
+ *   mean[n] = average of S over the channels and Omega of image n (fused-ssim
+ *   README, "Usage", returns this mean).
+ * The backward applies the adjoint of the blur (a "full" correlation) to the
+ * upstream gradients of the statistics and combines them by the chain rule of
+ * the TriSSIM README, "How it works":
+ *   grad_img1 = B^T(g_mu1) + 2 img1 B^T(g_s11) + img2 B^T(g_s12), grad_img2 likewise.
+ *
+ * Padding (fused-ssim README, "Usage"):
+ *   GBSSIM_VALID      Omega = (H-10) x (W-10): windows that lie inside the image.
+ *                     Needs H, W >= 11 (and D >= 11 in 3D).
+ *   GBSSIM_SAME_ZERO  Omega = H x W: the image is extended by zeros; border
+ *                     windows are not renormalised.  Needs H, W >= 1.
+ *
+ * Conventions shared by every call below:
+ *   - Images are contiguous float32, NCHW (2D) or NCDHW (3D), in DEVICE memory,
+ *     4-byte aligned.  Values are expected in [0, 1] but are not checked; NaN
+ *     propagates.
+ *   - All pointers are caller-owned.  The library allocates no memory and keeps
+ *     no state between calls except small per-device launch caches.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream.  Argument errors are returned before any
+ *     launch; a failed launch returns GBSSIM_ECUDA.
+ *   - Return value: GBSSIM_OK (0) or a negative status; nothing aborts.
+ *   - Calls are deterministic: the same inputs give bit-identical outputs.
+ */
+#ifndef GBSSIM_H
+#define GBSSIM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GBSSIM_ABI_VERSION 1
+
+typedef enum { GBSSIM_VALID = 0, GBSSIM_SAME_ZERO = 1 } gbssim_padding;
+
+enum {
+    GBSSIM_OK = 0,
+    GBSSIM_EINVAL = -1,     /* null pointer where one is required, bad enum, aliasing */
+    GBSSIM_ESHAPE = -2,     /* N, C < 1, a spatial extent too small, or sizes too large */
+    GBSSIM_EALIGN = -3,     /* a pointer not 4-byte aligned */
+    GBSSIM_EWORKSPACE = -4, /* workspace or saved buffer missing or too small */
+    GBSSIM_ECUDA = -5       /* a CUDA runtime call or launch failed */
+};
+
+/* ABI version of the loaded library (GBSSIM_ABI_VERSION at its build). */
+int gbssim_abi_version(void);
+
+/* A static, human-readable description of a status code. */
+const char *gbssim_strerror(int status);
+
+/* The eleven float32 taps the kernels use (host copy), w[0..10].  They are the
+ * float32 roundings of exp(-(k-5)^2 / 4.5), k = 0..10, divided by their sum. */
+void gbssim_window(float w[11]);
+
+/* ------------------------------------------------------------------ 2D ----- */
+
+/* Bytes of scratch that ssim_fwd needs for the given shape (per-block partial
+ * sums and a completion counter).  Returns 0 if the shape is invalid.  The
+ * buffer must be zero-filled once before its first use; every completed call
+ * leaves it zero-filled again.  Two calls that run at the same time must not
+ * share one workspace. */
+size_t gbssim_workspace_bytes(int N, int C, int H, int W, int padding);
+
+/* Bytes of the optional `saved` buffer of ssim_fwd: one float32 field the size
+ * of the input for grad_img1, plus one more when want_grad2 != 0. */
+size_t gbssim_saved_bytes(int N, int C, int H, int W, int want_grad2);
+
+/* Forward.
+ *   img1, img2       [N, C, H, W] float32, device.
+ *   out_mean         [N] float32, device: mean SSIM of each image.
+ *   out_map_or_null  [N, C, Ho, Wo] float32, device, or NULL: the SSIM map.
+ *   saved_or_null    device buffer of saved_bytes >= gbssim_saved_bytes(..., want_grad2),
+ *                    or NULL.  When given, the forward also computes, for each
+ *                    image, the gradient of mean[n] itself (i.e. with dL = 1)
+ *                    with respect to img1 (and img2 when want_grad2 != 0), so
+ *                    that ssim_bwd is a single scaling pass.  NULL is the
+ *                    inference mode ("train=False" of the fused-ssim README,
+ *                    "Usage"): only the mean (and map) are computed.
+ *   workspace        device buffer of workspace_bytes >= gbssim_workspace_bytes(...).
+ */
+int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+             float *out_mean, float *out_map_or_null, float *saved_or_null, size_t saved_bytes,
+             int want_grad2, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward of loss = sum_n dL[n] * mean[n] (dL = dLoss/dmean, [N] float32, device).
+ *   saved_or_null    the buffer written by a matching ssim_fwd (same images, shape
+ *                    and padding; want_grad2 set there if grad_img2 is wanted
+ *                    here), or NULL to recompute everything from img1 and img2.
+ *   grad_img1        [N, C, H, W] float32, device; overwritten (not accumulated).
+ *   grad_img2_or_null  likewise, or NULL to skip it (fused-ssim README,
+ *                    "Constraints": by default only img1 is differentiable).
+ * Gradient buffers must not overlap img1, img2 or each other. */
+int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int H, int W,
+             int padding, const float *saved_or_null, size_t saved_bytes, float *grad_img1,
+             float *grad_img2_or_null, void *stream);
+
+/* ------------------------------------------------------------------ 3D ----- */
+/* fused-ssim README, "3D data": the same statistics with an 11x11x11 window on
+ * NCDHW volumes.  Arguments mean what they mean in 2D, with D added. */
+
+size_t gbssim3d_workspace_bytes(int N, int C, int D, int H, int W, int padding);
+size_t gbssim3d_saved_bytes(int N, int C, int D, int H, int W, int want_grad2);
+
+int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
+               int padding, float *out_mean, float *out_map_or_null, float *saved_or_null,
+               size_t saved_bytes, int want_grad2, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int D,
+               int H, int W, int padding, const float *saved_or_null, size_t saved_bytes,
+               float *grad_img1, float *grad_img2_or_null, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBSSIM_H */

@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Every call goes through the C ABI (via the thin torch wrappers).  Bars, from
+the loss's specification: |mean_gpu - mean_oracle| <= 1e-5 for every image;
+max |grad_gpu - grad_oracle| <= 1e-4 * max |grad_oracle| for each gradient.
+The SSIM map has no stated bar; it is held to 2e-5 absolute (float32 window
+sums of values in [0, 1] carry ~1e-6 absolute error into S).
+"""
+import numpy as np
+import pytest
+
+from workloads import WORKLOADS, dl_vector, make_inputs, uniform_pair
+
+pytestmark = pytest.mark.gpu
+
+MEAN_TOL = 1e-5
+GRAD_RTOL = 1e-4
+MAP_TOL = 2e-5
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from differentiable_image_quality_gb300 import _abi, _build
+
+    _build.build()
+    _abi.load()
+    return torch.device("cuda:0")
+
+
+def _run(dev, x, y, dl, padding, want_grad2, path, want_map=False):
+    """One forward + backward through the C ABI; path 'saved' or 'recompute'."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    tx = torch.from_numpy(x).to(dev)
+    ty = torch.from_numpy(y).to(dev)
+    tdl = torch.from_numpy(np.ascontiguousarray(dl, dtype=np.float32)).to(dev)
+    N = x.shape[0]
+    is3d = x.ndim == 5
+    fwd = pkg.ssim3d_fwd if is3d else pkg.ssim_fwd
+    bwd = pkg.ssim3d_bwd if is3d else pkg.ssim_bwd
+    mean = torch.full((N,), float("nan"), device=dev)
+    smap = None
+    if want_map:
+        ext = [s - 10 if padding == "valid" else s for s in x.shape[2:]]
+        smap = torch.full((N, x.shape[1], *ext), float("nan"), device=dev)
+    saved = None
+    if path == "saved":
+        saved = torch.empty(pkg.saved_bytes(x.shape, want_grad2) // 4, device=dev)
+    fwd(tx, ty, padding, mean, out_map=smap, saved=saved, want_grad2=want_grad2)
+    g1 = torch.full_like(tx, float("nan"))
+    g2 = torch.full_like(ty, float("nan")) if want_grad2 else None
+    bwd(tdl, tx, ty, padding, g1, g2, saved=saved)
+    torch.cuda.synchronize()
+    out = {"mean": mean.cpu().numpy(), "g1": g1.cpu().numpy()}
+    if want_grad2:
+        out["g2"] = g2.cpu().numpy()
+    if want_map:
+        out["map"] = smap.cpu().numpy()
+    return out
+
+
+def _oracle(oracle_mod, x, y, dl, padding, want_grad2, want_map=False):
+    if x.ndim == 5:
+        mean = oracle_mod.ssim3d(x, y, padding, want_map=want_map)
+        g1, g2 = oracle_mod.ssim3d_grad(x, y, dl, padding, want_grad2)
+    else:
+        mean = oracle_mod.ssim2d(x, y, padding, want_map=want_map)
+        g1, g2 = oracle_mod.ssim2d_grad(x, y, dl, padding, want_grad2)
+    smap = None
+    if want_map:
+        mean, smap = mean
+    return {"mean": mean, "g1": g1, "g2": g2, "map": smap}
+
+
+def _assert_parity(got, ref, want_grad2, label=""):
+    dm = np.max(np.abs(got["mean"].astype(np.float64) - ref["mean"]))
+    assert dm <= MEAN_TOL, f"{label} mean off by {dm:.3e}"
+    for k in ("g1", "g2") if want_grad2 else ("g1",):
+        scale = np.max(np.abs(ref[k]))
+        err = np.max(np.abs(got[k].astype(np.float64) - ref[k])) / scale
+        assert np.all(np.isfinite(got[k])), f"{label} {k} has non-finite values"
+        assert err <= GRAD_RTOL, f"{label} {k} relative error {err:.3e}"
+    if "map" in got and ref.get("map") is not None:
+        dmap = np.max(np.abs(got["map"].astype(np.float64) - ref["map"]))
+        assert dmap <= MAP_TOL, f"{label} map off by {dmap:.3e}"
+
+
+SMALL_2D = [
+    # (shape, padding, seed) -- several strips (118 / 128 columns), ragged tails
+    ((1, 3, 64, 64), "valid", 1),
+    ((1, 3, 64, 64), "same", 2),
+    ((2, 2, 37, 301), "valid", 3),
+    ((2, 2, 37, 301), "same", 4),
+    ((1, 1, 250, 257), "valid", 5),
+    ((1, 1, 250, 257), "same", 6),
+    ((3, 1, 11, 11), "valid", 7),     # one output pixel per plane
+    ((1, 4, 11, 130), "valid", 8),
+    ((1, 1, 1, 1), "same", 9),
+    ((2, 1, 3, 1), "same", 10),
+    ((1, 2, 5, 139), "same", 11),
+    ((1, 1, 129, 12), "valid", 12),   # tall and narrow
+    ((1, 1, 130, 236), "same", 13),   # exactly two gradient strips
+]
+
+
+@pytest.mark.parametrize("path", ["saved", "recompute"])
+@pytest.mark.parametrize("shape,padding,seed", SMALL_2D)
+def test_parity_small_2d(dev, oracle_mod, shape, padding, seed, path):
+    x, y = uniform_pair(shape, 500 + seed, std=0.08)
+    dl = np.linspace(-1.0, 0.5, shape[0])
+    got = _run(dev, x, y, dl, padding, True, path, want_map=True)
+    ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
+    _assert_parity(got, ref, True, f"{shape} {padding} {path}")
+
+
+@pytest.mark.parametrize("seg_rows", [22, 23, 40, 57])
+@pytest.mark.parametrize("padding", ["valid", "same"])
+def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
+    """Short row segments: the 20-row warm-up and segment ownership of the mean."""
+    from differentiable_image_quality_gb300 import _abi
+
+    x, y = uniform_pair((2, 2, 97, 150), 600 + seg_rows, std=0.1)
+    dl = np.array([-1.0, -0.3])
+    lib = _abi.load()
+    lib.gbssim_tune_seg_rows(seg_rows)
+    try:
+        for path in ("saved", "recompute"):
+            got = _run(dev, x, y, dl, padding, True, path, want_map=True)
+            ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
+            _assert_parity(got, ref, True, f"seg_rows={seg_rows} {padding} {path}")
+    finally:
+        lib.gbssim_tune_seg_rows(0)
+
+
+@pytest.mark.parametrize("name", ["tiny64_valid", "splat1080_valid", "splat1080_same",
+                                  "batch512_valid"])
+@pytest.mark.parametrize("path", ["saved", "recompute"])
+def test_parity_workloads_2d(dev, oracle_mod, name, path):
+    wl = WORKLOADS[name]
+    x, y = make_inputs(name)
+    dl = dl_vector(name)
+    got = _run(dev, x, y, dl, wl.padding, wl.want_grad2, path)
+    ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2)
+    _assert_parity(got, ref, wl.want_grad2, f"{name} {path}")
+
+
+def test_deterministic_and_paths_agree(dev):
+    x, y = make_inputs("batch512_valid")
+    dl = dl_vector("batch512_valid")
+    a = _run(dev, x, y, dl, "valid", True, "saved")
+    b = _run(dev, x, y, dl, "valid", True, "saved")
+    c = _run(dev, x, y, dl, "valid", True, "recompute")
+    for k in ("mean", "g1", "g2"):
+        np.testing.assert_array_equal(a[k], b[k])
+    # the two paths differ only by where dL is applied (float32 rounding)
+    assert np.max(np.abs(a["g1"] - c["g1"])) <= 1e-6 * np.max(np.abs(a["g1"]))
+
+
+def test_identical_images(dev):
+    x, _ = uniform_pair((1, 3, 70, 90), 700)
+    for padding in ("valid", "same"):
+        got = _run(dev, x, x, [-1.0], padding, True, "saved", want_map=True)
+        assert abs(got["mean"][0] - 1.0) <= MEAN_TOL
+        assert np.max(np.abs(got["map"] - 1.0)) <= MAP_TOL
+        # the exact gradient is zero; the float32 one is rounding noise far below
+        # the typical gradient of a differing pair (~1e-6 per pixel here)
+        assert np.max(np.abs(got["g1"])) < 1e-8
+
+
+def test_outputs_stay_inside_their_buffers(dev):
+    """Guard bands around every output stay untouched (NaN sentinels elsewhere)."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    shape = (2, 3, 45, 140)
+    x, y = uniform_pair(shape, 701, std=0.1)
+    n = int(np.prod(shape))
+    guard = 4096
+    for padding in ("valid", "same"):
+        ho = shape[2] - 10 if padding == "valid" else shape[2]
+        wo = shape[3] - 10 if padding == "valid" else shape[3]
+        nmap = shape[0] * shape[1] * ho * wo
+        sentinel = 12345.0
+        tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+        big = torch.full((4 * guard + 2 * nmap + 2 * n + 8,), sentinel, device=dev)
+        mean = big[guard: guard + 2]
+        smap = big[2 * guard: 2 * guard + nmap].view(shape[0], shape[1], ho, wo)
+        saved = big[3 * guard + nmap: 3 * guard + nmap + 2 * n]
+        pkg.ssim_fwd(tx, ty, padding, mean, out_map=smap, saved=saved, want_grad2=True)
+        g = torch.full((2 * guard + 2 * n,), sentinel, device=dev)
+        g1 = g[guard: guard + n].view(shape)
+        g2 = g[guard + n: guard + 2 * n].view(shape)
+        pkg.ssim_bwd(torch.tensor([-1.0, 2.0], device=dev), tx, ty, padding, g1, g2)
+        torch.cuda.synchronize()
+        hb = big.cpu().numpy()
+        assert np.all(hb[:guard] == sentinel) and np.all(hb[guard + 2: 2 * guard] == sentinel)
+        assert np.all(hb[2 * guard + nmap: 3 * guard + nmap] == sentinel)
+        assert np.all(hb[3 * guard + nmap + 2 * n:] == sentinel)
+        hg = g.cpu().numpy()
+        assert np.all(hg[:guard] == sentinel) and np.all(hg[guard + 2 * n:] == sentinel)
+        assert np.all(np.isfinite(hb[2 * guard: 2 * guard + nmap]))
+
+
+def test_autograd_api(dev, oracle_mod):
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    x, y = uniform_pair((2, 3, 48, 61), 702, std=0.1)
+    for padding in ("valid", "same"):
+        for train in (True, False):
+            tx = torch.from_numpy(x).to(dev).requires_grad_(True)
+            ty = torch.from_numpy(y).to(dev).requires_grad_(True)
+            loss = 1.0 - pkg.fused_ssim(tx, ty, padding=padding, train=train)
+            loss.backward()
+            ref_mean = oracle_mod.ssim2d(x, y, padding)
+            g1, g2 = oracle_mod.ssim2d_grad(x, y, [-0.5, -0.5], padding)
+            assert abs(loss.item() - (1 - ref_mean.mean())) <= MEAN_TOL
+            for got, ref in ((tx.grad, g1), (ty.grad, g2)):
+                err = np.max(np.abs(got.cpu().numpy() - ref)) / np.max(np.abs(ref))
+                assert err <= GRAD_RTOL
+    with torch.no_grad():
+        tx = torch.from_numpy(x).to(dev)
+        m = pkg.fused_ssim(tx, tx, padding="valid", train=False, per_image=True)
+    assert m.shape == (2,) and torch.all(torch.abs(m - 1) <= MEAN_TOL)
+
+
+def test_python_api_errors(dev):
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    a = torch.rand(1, 1, 32, 32, device=dev)
+    with pytest.raises(TypeError):
+        pkg.fused_ssim(a.double(), a.double())
+    with pytest.raises(ValueError):
+        pkg.fused_ssim(a, a[:, :, :31])
+    with pytest.raises(ValueError):
+        pkg.fused_ssim(a.transpose(2, 3), a)
+    with pytest.raises(pkg.GbssimError):
+        pkg.fused_ssim(a[:, :, :10], a[:, :, :10].clone(), padding="valid")
