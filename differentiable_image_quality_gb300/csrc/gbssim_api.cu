@@ -166,6 +166,8 @@ const char *gbssim_strerror(int status)
     case GBSSIM_EALIGN: return "misaligned pointer (float32 buffers need 4-byte alignment)";
     case GBSSIM_EWORKSPACE: return "workspace or saved buffer missing or too small";
     case GBSSIM_ECUDA: return "a CUDA runtime call or kernel launch failed";
+    case GBSSIM_ETOOLARGE:
+        return "problem too large for the fixed scratch of ssim_fwd_noalloc (use ssim_fwd)";
     default: return "unknown status";
     }
 }

@@ -52,7 +52,8 @@ enum {
     GBSSIM_ESHAPE = -2,     /* N, C < 1, a spatial extent too small, or sizes too large */
     GBSSIM_EALIGN = -3,     /* a pointer not 4-byte aligned */
     GBSSIM_EWORKSPACE = -4, /* workspace or saved buffer missing or too small */
-    GBSSIM_ECUDA = -5       /* a CUDA runtime call or launch failed */
+    GBSSIM_ECUDA = -5,      /* a CUDA runtime call or launch failed */
+    GBSSIM_ETOOLARGE = -6   /* too large for the fixed scratch of ssim_fwd_noalloc */
 };
 
 /* ABI version of the loaded library (GBSSIM_ABI_VERSION at its build). */
@@ -106,6 +107,32 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
 int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int H, int W,
              int padding, const float *saved_or_null, size_t saved_bytes, float *grad_img1,
              float *grad_img2_or_null, void *stream);
+
+/* Size of the device array behind ssim_fwd_noalloc (per GPU, for the process's life). */
+#define GBSSIM_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* ssim_fwd for callers that cannot allocate device memory.  The pages describe
+ * no such call; it exists for users of this library.  A plug-in running inside
+ * an application that owns the device memory, or code on a latency-critical
+ * path that must not call cudaMalloc (which can also synchronise the device),
+ * cannot provide ssim_fwd's workspace.  This call takes the same arguments minus
+ * the workspace and uses a fixed array that the library defines in device
+ * memory instead: GBSSIM_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ * library, held until the process exits.  It allocates nothing.
+ *   - Shapes whose workspace (gbssim_workspace_bytes) would exceed that array
+ *     return GBSSIM_ETOOLARGE; use ssim_fwd for them.  A 1 x 3 x 1080 x 1920
+ *     pair needs about 20 KB of it.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents; the call clears the part that must start at zero.  Calls
+ *     whose work overlaps on the GPU (other streams, other threads) race on it:
+ *     order them on one stream.
+ *   - The first call on each device looks up the array's device address (and
+ *     does the per-device set-up ssim_fwd also does); make that first call
+ *     before any stream capture.
+ * Results are identical to ssim_fwd's. */
+int ssim_fwd_noalloc(const float *img1, const float *img2, int N, int C, int H, int W,
+                     int padding, float *out_mean, float *out_map_or_null, float *saved_or_null,
+                     size_t saved_bytes, int want_grad2, void *stream);
 
 /* ------------------------------------------------------------------ 3D ----- */
 /* fused-ssim README, "3D data": the same statistics with an 11x11x11 window on
