@@ -98,9 +98,10 @@ _ws_cache: dict = {}
 
 
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A zero-filled scratch buffer per device, grown on demand.  The library
-    leaves it zero-filled after every completed call.  Calls on concurrent
-    streams of one device must pass their own buffers to the low-level API."""
+    """A zero-filled scratch buffer per device, grown on demand (256-byte
+    aligned, as the caching allocator returns).  The library leaves its counter
+    zero after every completed call.  Calls on concurrent streams of one device
+    must pass their own buffers to the low-level API."""
     key = (device.type, device.index)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
@@ -155,14 +156,19 @@ def ssim3d_fwd(img1, img2, padding, out_mean, out_map=None, saved=None, want_gra
     _abi.check("ssim3d_fwd", st)
 
 
-def ssim3d_bwd(dL, img1, img2, padding, grad1, grad2=None, saved=None):
+def ssim3d_bwd(dL, img1, img2, padding, grad1, grad2=None, saved=None, workspace=None):
     _check_pair(img1, img2, 3)
     N, C, D, H, W = img1.shape
+    pad = _pad(padding)
     lib = _abi.load()
-    st = lib.ssim3d_bwd(_abi.ptr(dL), _abi.ptr(img1), _abi.ptr(img2), N, C, D, H, W,
-                        _pad(padding), _abi.ptr(saved),
+    if saved is None and workspace is None:
+        workspace = _workspace(img1.device, int(lib.gbssim3d_workspace_bytes(N, C, D, H, W, pad)))
+    st = lib.ssim3d_bwd(_abi.ptr(dL), _abi.ptr(img1), _abi.ptr(img2), N, C, D, H, W, pad,
+                        _abi.ptr(saved),
                         0 if saved is None else saved.numel() * saved.element_size(),
-                        _abi.ptr(grad1), _abi.ptr(grad2), _stream(img1))
+                        _abi.ptr(grad1), _abi.ptr(grad2), _abi.ptr(workspace),
+                        0 if workspace is None else workspace.numel() * workspace.element_size(),
+                        _stream(img1))
     _abi.check("ssim3d_bwd", st)
 
 

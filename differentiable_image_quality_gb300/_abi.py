@@ -32,7 +32,8 @@ SIGNATURES = {
     "gbssim3d_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gbssim3d_saved_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "ssim3d_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),
-    "ssim3d_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp]),
+    "ssim3d_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp, _sz,
+                        _vp]),
 }
 # exported beyond the header: the planner's tuning hook
 EXTRA = {"gbssim_tune_seg_rows": (None, [_i])}

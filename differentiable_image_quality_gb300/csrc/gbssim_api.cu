@@ -21,6 +21,7 @@ struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
+    int occ3d[2] = {0, 0};     // statistics kernel, adjoint kernel
 };
 
 std::mutex g_mutex;
@@ -55,8 +56,8 @@ int device_info(DeviceInfo **out)
             if (e != cudaSuccess) return cuda_fail(e);
             if (d.occ2d[i] < 1) return cuda_fail(cudaErrorInvalidConfiguration);
         }
-        int rc = ssim3d_prepare_device();
-        if (rc != GBSSIM_OK) return rc;
+        const cudaError_t e3 = ssim3d_prepare(d.occ3d);
+        if (e3 != cudaSuccess) return cuda_fail(e3);
         d.ready = true;
     }
     *out = &d;
@@ -149,6 +150,74 @@ bool shape2d_ok(int N, int C, int H, int W, int padding)
     if ((long long)N * C > INT_MAX) return false;
     if (H > (1 << 28) || W > (1 << 28)) return false;
     return true;
+}
+
+// ---- 3D
+
+constexpr int kMinZSeg = 12;  // shortest z segment the planner uses
+
+bool shape3d_ok(int N, int C, int D, int H, int W, int padding)
+{
+    if (N < 1 || C < 1) return false;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return false;
+    if (!extent_ok(D, padding) || !extent_ok(H, padding) || !extent_ok(W, padding)) return false;
+    if ((long long)N * C > INT_MAX) return false;
+    if (D > (1 << 20) || H > (1 << 20) || W > (1 << 20)) return false;
+    return true;
+}
+
+struct Plan3d {
+    int tiles_x = 0, tiles_y = 0, zsegs = 0, zseg_len = 0;
+    long long blocks = 0;
+};
+
+// Tiles of 16 x 32 columns over (rows, cols), z segments over zlen, with the
+// same per-SM cost model as in 2D (a 10-slice warm-up per segment).
+Plan3d plan3d(long long planes, int zlen, int rows, int cols, int sm_count, int occ)
+{
+    Plan3d p;
+    p.tiles_x = int(ceil_div(cols, kTile3dX));
+    p.tiles_y = int(ceil_div(rows, kTile3dY));
+    const long long per_z = planes * p.tiles_x * p.tiles_y;
+    const int sat = occ < 2 ? occ : 2;
+    const int max_segs = int(ceil_div(zlen, kMinZSeg));
+    double best = -1.0;
+    long long best_work = 0;
+    for (int s = 1; s <= max_segs; ++s) {
+        const int len = int(ceil_div(zlen, s));
+        const int segs = int(ceil_div(zlen, len));
+        const long long blocks = per_z * segs;
+        const long long steps = len + 10;
+        const long long per_sm = ceil_div(blocks, (long long)sm_count);
+        const double eff = double(per_sm < sat ? per_sm : sat) / sat;
+        const double cost = double(per_sm * steps) / eff;
+        const long long work = blocks * steps;
+        if (best < 0 || cost < best - 1e-9 || (cost <= best + 1e-9 && work < best_work)) {
+            best = cost;
+            best_work = work;
+            p.zsegs = segs;
+            p.zseg_len = len;
+            p.blocks = blocks;
+        }
+    }
+    return p;
+}
+
+struct Layout3d {
+    size_t partials_off, gfield_off, total;
+};
+
+Layout3d layout3d(int N, int C, int D, int H, int W, int padding)
+{
+    const long long planes = (long long)N * C;
+    const int Do = out_extent(D, padding), Ho = out_extent(H, padding), Wo = out_extent(W, padding);
+    const long long maxb = planes * ceil_div(Wo, kTile3dX) * ceil_div(Ho, kTile3dY) *
+                           ceil_div(Do, kMinZSeg);
+    Layout3d l;
+    l.partials_off = kCounterBytes;
+    l.gfield_off = size_t(ceil_div((long long)(kCounterBytes + maxb * sizeof(double)), 256)) * 256;
+    l.total = l.gfield_off + size_t(planes) * Do * Ho * Wo * 4 * sizeof(float);
+    return l;
 }
 
 }  // namespace
@@ -314,6 +383,149 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     a.blocks_per_image = int(p.blocks / N);
     a.count = double(C) * double(Ho) * double(Wo);
     return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), s));
+}
+
+
+size_t gbssim3d_workspace_bytes(int N, int C, int D, int H, int W, int padding)
+{
+    if (!shape3d_ok(N, C, D, H, W, padding)) return 0;
+    return layout3d(N, C, D, H, W, padding).total;
+}
+
+size_t gbssim3d_saved_bytes(int N, int C, int D, int H, int W, int want_grad2)
+{
+    if (N < 1 || C < 1 || D < 1 || H < 1 || W < 1) return 0;
+    const size_t field = size_t(N) * C * D * H * W * sizeof(float);
+    return want_grad2 ? 2 * field : field;
+}
+
+static void fill3d(Ssim3dArgs &a, const float *x, const float *y, int N, int C, int D, int H,
+                   int W, int padding, void *workspace)
+{
+    a.x = x; a.y = y;
+    a.D = D; a.H = H; a.W = W;
+    a.Do = out_extent(D, padding); a.Ho = out_extent(H, padding); a.Wo = out_extent(W, padding);
+    a.off = padding == GBSSIM_VALID ? 0 : kRadius;
+    a.C = C;
+    const Layout3d l = layout3d(N, C, D, H, W, padding);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.counter = reinterpret_cast<unsigned *>(ws);
+    a.gfield = reinterpret_cast<float *>(ws + l.gfield_off);
+    a.inv_count = float(1.0 / (double(C) * a.Do * a.Ho * a.Wo));
+    a.count = double(C) * a.Do * a.Ho * a.Wo;
+    a.images = N;
+}
+
+static void apply_plan(Ssim3dArgs &a, const Plan3d &p)
+{
+    a.tiles_x = p.tiles_x; a.tiles_y = p.tiles_y; a.zsegs = p.zsegs; a.zseg_len = p.zseg_len;
+}
+
+int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
+               int padding, float *out_mean, float *out_map_or_null, float *saved_or_null,
+               size_t saved_bytes, int want_grad2, void *workspace, size_t workspace_bytes,
+               void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_mean)) ||
+        (rc = check_opt(out_map_or_null)) || (rc = check_opt(saved_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape3d_ok(N, C, D, H, W, padding)) return GBSSIM_ESHAPE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return GBSSIM_EWORKSPACE;
+    if (workspace_bytes < gbssim3d_workspace_bytes(N, C, D, H, W, padding)) return GBSSIM_EWORKSPACE;
+    const bool grad = saved_or_null != nullptr;
+    const size_t img_bytes = size_t(N) * C * D * H * W * sizeof(float);
+    if (grad && saved_bytes < gbssim3d_saved_bytes(N, C, D, H, W, want_grad2))
+        return GBSSIM_EWORKSPACE;
+    if (grad && (overlaps(saved_or_null, saved_bytes, img1, img_bytes) ||
+                 overlaps(saved_or_null, saved_bytes, img2, img_bytes) ||
+                 overlaps(saved_or_null, saved_bytes, workspace, workspace_bytes)))
+        return GBSSIM_EINVAL;
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Ssim3dArgs a{};
+    fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
+    if (pa.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    apply_plan(a, pa);
+    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
+    a.mean = out_mean;
+    a.map = out_map_or_null;
+    a.blocks_per_image = int(pa.blocks / N);
+    cudaError_t e = ssim3d_stats_launch(a, grad, int(pa.blocks), s);
+    if (e != cudaSuccess || !grad) return cuda_fail(e);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    if (pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    apply_plan(a, pb);
+    a.out1 = saved_or_null;
+    a.out2 = want_grad2 ? saved_or_null + size_t(N) * C * D * H * W : nullptr;
+    a.dL = nullptr;
+    return cuda_fail(ssim3d_adjoint_launch(a, want_grad2 != 0, int(pb.blocks), s));
+}
+
+int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int D,
+               int H, int W, int padding, const float *saved_or_null, size_t saved_bytes,
+               float *grad_img1, float *grad_img2_or_null, void *workspace,
+               size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_in(dL)) || (rc = check_in(img1)) || (rc = check_in(img2)) ||
+        (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)) ||
+        (rc = check_opt(saved_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape3d_ok(N, C, D, H, W, padding)) return GBSSIM_ESHAPE;
+    const size_t total = size_t(N) * C * D * H * W;
+    const size_t img_bytes = total * sizeof(float);
+    const bool g2 = grad_img2_or_null != nullptr;
+    if (overlaps(grad_img1, img_bytes, img1, img_bytes) ||
+        overlaps(grad_img1, img_bytes, img2, img_bytes) ||
+        overlaps(grad_img1, img_bytes, dL, size_t(N) * sizeof(float)) ||
+        (g2 && (overlaps(grad_img2_or_null, img_bytes, img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, img2, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, dL, size_t(N) * sizeof(float)) ||
+                overlaps(grad_img2_or_null, img_bytes, grad_img1, img_bytes))))
+        return GBSSIM_EINVAL;
+    const float *f1 = saved_or_null, *f2 = (saved_or_null && g2) ? saved_or_null + total : nullptr;
+    if (saved_or_null) {
+        if (saved_bytes < gbssim3d_saved_bytes(N, C, D, H, W, g2)) return GBSSIM_EWORKSPACE;
+        if ((overlaps(grad_img1, img_bytes, saved_or_null, saved_bytes) && grad_img1 != f1) ||
+            (g2 && overlaps(grad_img2_or_null, img_bytes, saved_or_null, saved_bytes) &&
+             grad_img2_or_null != f2))
+            return GBSSIM_EINVAL;
+    } else {
+        if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+            workspace_bytes < gbssim3d_workspace_bytes(N, C, D, H, W, padding))
+            return GBSSIM_EWORKSPACE;
+        if (overlaps(grad_img1, img_bytes, workspace, workspace_bytes) ||
+            (g2 && overlaps(grad_img2_or_null, img_bytes, workspace, workspace_bytes)))
+            return GBSSIM_EINVAL;
+    }
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (saved_or_null)
+        return cuda_fail(scale_fields_launch(f1, f2, grad_img1, grad_img2_or_null, dL, 1.0f,
+                                             size_t(C) * D * H * W, total, d->sm_count, s));
+    Ssim3dArgs a{};
+    fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    apply_plan(a, pa);
+    a.partials = nullptr;
+    a.map = nullptr;
+    cudaError_t e = ssim3d_stats_launch(a, true, int(pa.blocks), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    apply_plan(a, pb);
+    a.out1 = grad_img1;
+    a.out2 = grad_img2_or_null;
+    a.dL = dL;
+    return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pb.blocks), s));
 }
 
 }  // extern "C"

@@ -136,9 +136,18 @@ int ssim_fwd_noalloc(const float *img1, const float *img2, int N, int C, int H, 
 
 /* ------------------------------------------------------------------ 3D ----- */
 /* fused-ssim README, "3D data": the same statistics with an 11x11x11 window on
- * NCDHW volumes.  Arguments mean what they mean in 2D, with D added. */
+ * NCDHW volumes.  Arguments mean what they mean in 2D, with D added; both
+ * paddings apply to all three axes (valid needs D, H, W >= 11).
+ * The 3D calls keep the per-voxel derivatives of SSIM between their two
+ * kernels in the workspace, so ssim3d_bwd takes one too (it is only used when
+ * saved_or_null is NULL). */
 
+/* Workspace bytes of ssim3d_fwd / ssim3d_bwd (0 for an invalid shape).  Same
+ * zero-fill rule as gbssim_workspace_bytes. */
 size_t gbssim3d_workspace_bytes(int N, int C, int D, int H, int W, int padding);
+
+/* Bytes of the optional saved buffer (one field the size of the input per
+ * wanted gradient). */
 size_t gbssim3d_saved_bytes(int N, int C, int D, int H, int W, int want_grad2);
 
 int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
@@ -148,7 +157,8 @@ int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H,
 
 int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int D,
                int H, int W, int padding, const float *saved_or_null, size_t saved_bytes,
-               float *grad_img1, float *grad_img2_or_null, void *stream);
+               float *grad_img1, float *grad_img2_or_null, void *workspace,
+               size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

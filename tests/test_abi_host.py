@@ -128,3 +128,30 @@ def test_python_api_rejects_cpu_tensors():
     x = torch.zeros(1, 1, 16, 16)
     with pytest.raises(TypeError):
         pkg.fused_ssim(x, x)
+
+
+def test_3d_argument_errors(lib):
+    n = 1 * 1 * 12 * 12 * 12 * 4
+    ws = lib.gbssim3d_workspace_bytes(1, 1, 12, 12, 12, 0)
+    assert ws > 2 * 2 * 2 * 16  # derivative fields of the 2x2x2 output domain
+    assert lib.gbssim3d_workspace_bytes(1, 1, 10, 12, 12, 0) == 0
+    assert lib.gbssim3d_saved_bytes(1, 1, 12, 12, 12, 1) == 2 * n
+
+    def fwd(D=12, pad=0, wsp=FAKE * 256, wsb=ws, saved=None, sb=0):
+        return lib.ssim3d_fwd(1 << 30, 2 << 30, 1, 1, D, 12, 12, pad, 3 << 30, None, saved, sb, 0,
+                              wsp, wsb, None)
+
+    assert fwd(D=10) == ESHAPE
+    assert fwd(pad=2) == EINVAL
+    assert fwd(wsb=ws - 1) == EWORKSPACE
+    assert fwd(wsp=FAKE * 256 + 16) == EWORKSPACE  # workspace must be 256-byte aligned
+    assert fwd(saved=4 << 30, sb=n - 4) == EWORKSPACE
+
+    def bwd(wsp=FAKE * 256, wsb=ws, saved=None, sb=0, g1=5 << 30):
+        return lib.ssim3d_bwd(FAKE, 1 << 30, 2 << 30, 1, 1, 12, 12, 12, 0, saved, sb, g1, None,
+                              wsp, wsb, None)
+
+    assert bwd(wsp=None) == EWORKSPACE
+    assert bwd(wsb=ws - 1) == EWORKSPACE
+    assert bwd(g1=(1 << 30) + 4) == EINVAL
+    assert bwd(saved=4 << 30, sb=n - 4, wsp=None) == EWORKSPACE

@@ -139,15 +139,55 @@ def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
 
 
 @pytest.mark.parametrize("name", ["tiny64_valid", "splat1080_valid", "splat1080_same",
-                                  "batch512_valid"])
+                                  "batch512_valid", "volume128_valid"])
 @pytest.mark.parametrize("path", ["saved", "recompute"])
-def test_parity_workloads_2d(dev, oracle_mod, name, path):
+def test_parity_workloads(dev, oracle_mod, name, path):
     wl = WORKLOADS[name]
     x, y = make_inputs(name)
     dl = dl_vector(name)
     got = _run(dev, x, y, dl, wl.padding, wl.want_grad2, path)
     ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2)
     _assert_parity(got, ref, wl.want_grad2, f"{name} {path}")
+
+
+SMALL_3D = [
+    ((1, 1, 11, 11, 11), "valid", 1),
+    ((1, 1, 12, 12, 12), "valid", 2),
+    ((2, 2, 13, 19, 37), "valid", 3),
+    ((1, 2, 9, 17, 40), "same", 4),
+    ((2, 1, 30, 21, 45), "same", 5),    # several z segments, two tile columns
+    ((1, 1, 40, 36, 70), "valid", 6),   # ragged tiles (16 x 32) in both directions
+    ((1, 1, 1, 1, 1), "same", 7),
+    ((1, 1, 3, 40, 2), "same", 8),
+]
+
+
+@pytest.mark.parametrize("path", ["saved", "recompute"])
+@pytest.mark.parametrize("shape,padding,seed", SMALL_3D)
+def test_parity_small_3d(dev, oracle_mod, shape, padding, seed, path):
+    x, y = uniform_pair(shape, 800 + seed, std=0.08)
+    dl = np.linspace(-1.0, 0.5, shape[0])
+    got = _run(dev, x, y, dl, padding, True, path, want_map=True)
+    ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
+    _assert_parity(got, ref, True, f"{shape} {padding} {path}")
+
+
+def test_autograd_api_3d(dev, oracle_mod):
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    x, y = uniform_pair((1, 2, 14, 15, 16), 703, std=0.1)
+    for padding in ("valid", "same"):
+        tx = torch.from_numpy(x).to(dev).requires_grad_(True)
+        ty = torch.from_numpy(y).to(dev)
+        loss = 1.0 - pkg.fused_ssim3d(tx, ty, padding=padding)
+        loss.backward()
+        ref_mean = oracle_mod.ssim3d(x, y, padding)
+        g1, _ = oracle_mod.ssim3d_grad(x, y, [-1.0], padding, want_grad2=False)
+        assert abs(loss.item() - (1 - ref_mean[0])) <= MEAN_TOL
+        err = np.max(np.abs(tx.grad.cpu().numpy() - g1)) / np.max(np.abs(g1))
+        assert err <= GRAD_RTOL
 
 
 def test_deterministic_and_paths_agree(dev):
