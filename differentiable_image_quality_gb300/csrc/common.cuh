@@ -46,6 +46,16 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool in_
                  : "memory");
 }
 
+// 16-byte copy (global and shared addresses 16-byte aligned), L2 only.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool in_bounds)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int src_bytes = in_bounds ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -55,6 +65,16 @@ template <int Pending>
 __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(Pending) : "memory");
+}
+
+// Approximate reciprocal (the hardware instruction, relative error ~1 ulp).
+// Its argument here is a product of two sums each >= C1 or C2, never zero,
+// infinite or subnormal.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // ------------------------------------------------------------ SSIM at a pixel
@@ -85,7 +105,7 @@ __device__ __forceinline__ float ssim_value(const Moments &m)
     const float A2 = 2.0f * s12 + kC2;
     const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
     const float B2 = ss + kC2;
-    return __fdividef(A1 * A2, B1 * B2);
+    return A1 * A2 * rcp_approx(B1 * B2);
 }
 
 // S and its derivatives with respect to the shifted moments.
@@ -102,7 +122,7 @@ __device__ __forceinline__ float ssim_and_grads(const Moments &m, MomentGrads &g
     const float A2 = 2.0f * s12 + kC2;
     const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
     const float B2 = ss + kC2;
-    const float inv = __fdividef(1.0f, B1 * B2);
+    const float inv = rcp_approx(B1 * B2);
     const float S = A1 * A2 * inv;
     const float d_ss = -S * B1 * inv;      // -S / B2
     const float d_s12 = 2.0f * A1 * inv;
@@ -139,7 +159,8 @@ __device__ __forceinline__ double block_sum(float v, double *scratch /* NT/32 do
 
 // Grid-wide finish of the per-image means.  Every block calls this once, with
 // its partial sum already written to partials[blockIdx.x] by thread 0.  The
-// last block to arrive sums each image's partials in block order (double) and
+// last block to arrive sums each image's partials (double, a fixed assignment of
+// partials to threads and a fixed-order block reduction: deterministic) and
 // writes mean[n] = sum / count, then resets the counter to zero for the next
 // call.  blocks_per_image consecutive blocks belong to one image.
 template <int NT>
@@ -147,6 +168,7 @@ __device__ __forceinline__ void finish_means(double *partials, unsigned *counter
                                              int images, int blocks_per_image, double count)
 {
     __shared__ bool last;
+    __shared__ double wsum[NT / 32];
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned total = gridDim.x;
@@ -156,11 +178,22 @@ __device__ __forceinline__ void finish_means(double *partials, unsigned *counter
     __syncthreads();
     if (!last) return;
     __threadfence();
-    for (int n = threadIdx.x; n < images; n += NT) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int n = 0; n < images; ++n) {
         const double *p = partials + static_cast<size_t>(n) * blocks_per_image;
         double s = 0.0;
-        for (int b = 0; b < blocks_per_image; ++b) s += __ldcg(p + b);
-        mean[n] = static_cast<float>(s / count);
+        for (int b = threadIdx.x; b < blocks_per_image; b += NT) s += __ldcg(p + b);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) wsum[warp] = s;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) t += wsum[w];
+            mean[n] = static_cast<float>(t / count);
+        }
+        __syncthreads();
     }
     if (threadIdx.x == 0) *counter = 0u;
 }

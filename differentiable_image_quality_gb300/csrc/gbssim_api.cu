@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/gbssim.h"
+#include "gbssim.h"
 #include "common.cuh"
 #include "ssim2d.cuh"
 #include "ssim3d.cuh"
@@ -48,7 +48,7 @@ int device_info(DeviceInfo **out)
         const bool grad[3] = {false, true, true}, g2[3] = {false, false, true};
         for (int i = 0; i < 3; ++i) {
             const void *k = ssim2d_kernel_ptr(grad[i], g2[i]);
-            const size_t smem = ssim2d_smem_bytes(grad[i]);
+            const size_t smem = ssim2d_smem_bytes(grad[i], g2[i]);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  int(smem));
             if (e != cudaSuccess) return cuda_fail(e);
@@ -97,18 +97,41 @@ struct Plan2d {
     long long blocks = 0;
 };
 
-// Pick the row segmentation.  Time is modelled per SM: the busiest SM holds
-// ceil(blocks / SMs) blocks of `steps` row steps each, and an SM with fewer than
-// two resident blocks runs at a proportionally lower rate.
-Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, bool grad, int sm_count, int occ)
+// Relative SM throughput with k resident CTAs (k = 1, 2, 3, 4+), measured on the
+// 1080p workload: one 4-warp CTA alone leaves the SM about half idle.
+double occupancy_eff(int k)
+{
+    static const double e[4] = {0.5, 0.8, 1.0, 1.05};
+    return e[k < 1 ? 0 : (k > 4 ? 3 : k - 1)];
+}
+
+// Time of `blocks` CTAs of `steps` row steps each, in units of one CTA-step at
+// full occupancy: the grid runs in waves of SMs x occ CTAs; a wave whose
+// busiest SM holds k CTAs takes k (steps + 1) / eff(k) (the +1 is a CTA's fixed
+// start-up and finish).
+double wave_cost(long long blocks, long long steps, int sm_count, int occ)
+{
+    const long long slots = (long long)sm_count * occ;
+    double cost = 0.0;
+    while (blocks > 0) {
+        const long long in_wave = blocks < slots ? blocks : slots;
+        const int k = int(ceil_div(in_wave, sm_count));
+        cost += double(k) * double(steps + 1) / occupancy_eff(k);
+        blocks -= in_wave;
+    }
+    return cost;
+}
+
+// Pick the row segmentation: a gradient-mode segment walks seg_rows + 20 input
+// rows, a forward-only one seg_rows + 10.
+Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad, int sm_count,
+              int occ)
 {
     Plan2d p;
-    const int cols = grad ? W : Wo;
     const int rows = grad ? H : Ho;
     const int halo = grad ? 20 : 10;
-    p.strips = int(ceil_div(cols, grad ? ssim2d_grad_cols() : ssim2d_stat_cols()));
+    p.strips = ssim2d_strips(grad, W, Wo, off);
     const long long cols_planes = (long long)p.strips * planes;
-    const int sat = occ < 2 ? occ : 2;
     const int max_segs = int(ceil_div(rows, kMinSegRows));
     double best = -1.0;
     long long best_work = 0;
@@ -118,9 +141,7 @@ Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, bool grad, int sm_
         const int segs = int(ceil_div(rows, sr));
         const long long blocks = cols_planes * segs;
         const long long steps = ceil_div(sr + halo, kTaps);
-        const long long per_sm = ceil_div(blocks, sm_count);
-        const double eff = double(per_sm < sat ? per_sm : sat) / sat;
-        const double cost = double(per_sm * steps) / eff;
+        const double cost = wave_cost(blocks, steps, sm_count, occ);
         const long long work = blocks * steps;
         if (best < 0 || cost < best - 1e-9 || (cost <= best + 1e-9 && work < best_work)) {
             best = cost;
@@ -135,10 +156,10 @@ Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, bool grad, int sm_
 }
 
 // Upper bound of blocks over every plan (segments never shorter than kMinSegRows).
-long long max_blocks2d(long long planes, int H, int W, int Ho, int Wo)
+long long max_blocks2d(long long planes, int H, int W, int Ho, int Wo, int off)
 {
-    const long long g = ceil_div(W, ssim2d_grad_cols()) * ceil_div(H, kMinSegRows);
-    const long long f = ceil_div(Wo, ssim2d_stat_cols()) * ceil_div(Ho, kMinSegRows);
+    const long long g = ssim2d_strips(true, W, Wo, off) * ceil_div(H, kMinSegRows);
+    const long long f = ssim2d_strips(false, W, Wo, off) * ceil_div(Ho, kMinSegRows);
     return planes * (g > f ? g : f);
 }
 
@@ -259,7 +280,7 @@ size_t gbssim_workspace_bytes(int N, int C, int H, int W, int padding)
 {
     if (!shape2d_ok(N, C, H, W, padding)) return 0;
     const long long b = max_blocks2d((long long)N * C, H, W, out_extent(H, padding),
-                                     out_extent(W, padding));
+                                     out_extent(W, padding), padding == GBSSIM_VALID ? 0 : kRadius);
     return kCounterBytes + size_t(b) * sizeof(double);
 }
 
@@ -295,7 +316,8 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     DeviceInfo *d = nullptr;
     if ((rc = device_info(&d))) return rc;
     const int occ = d->occ2d[grad ? (want_grad2 ? 2 : 1) : 0];
-    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, grad, d->sm_count, occ);
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, grad, d->sm_count, occ);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
         return GBSSIM_EWORKSPACE;
@@ -303,9 +325,11 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
-    a.off = padding == GBSSIM_VALID ? 0 : kRadius;
+    a.off = off;
     a.C = C;
     a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     a.out1 = grad ? saved_or_null : nullptr;
     a.out2 = (grad && want_grad2) ? saved_or_null + size_t(N) * C * H * W : nullptr;
     a.dL = nullptr;
@@ -363,14 +387,17 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
         return cuda_fail(scale_fields_launch(f1, f2, grad_img1, grad_img2_or_null, dL, 1.0f,
                                              size_t(C) * H * W, total, d->sm_count, s));
     const int occ = d->occ2d[g2 ? 2 : 1];
-    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, true, d->sm_count, occ);
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count, occ);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
-    a.off = padding == GBSSIM_VALID ? 0 : kRadius;
+    a.off = off;
     a.C = C;
     a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     a.out1 = grad_img1;
     a.out2 = grad_img2_or_null;
     a.dL = dL;

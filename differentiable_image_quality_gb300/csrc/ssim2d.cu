@@ -11,17 +11,24 @@
 //
 // Design.  A CTA owns a vertical strip of columns of one (n, c) plane and walks
 // down a segment of its rows, 11 rows per step.  Per step:
-//   H  row pass: 11 input rows (staged in shared memory by cp.async, three
+//   H  row pass: 11 input rows (staged in shared memory by cp.async, two
 //      buffers) -> the four row-blurred statistics of 128 columns (hb);
 //   V  column pass, one thread per column: an 11-row register ring of hb gives
 //      the window statistics, then SSIM and its derivatives in registers; in
 //      gradient mode a second 11-row register ring of those derivatives gives
 //      the column pass of the adjoint (vb);
-//   A  row pass of the adjoint over vb, the chain rule with the input pixel, and
-//      the store of the gradient row.
+//   A  row pass of the adjoint over vb and the chain rule with the input pixel
+//      (re-read from L1 / L2); the gradient row is staged in shared memory and
+//      stored, one column per thread, during the next V.
 // H of step t+1 and A of step t share one barrier interval.  Streaming down the
 // rows computes every statistic of the strip once (no vertical halo recompute
 // except the 20-row warm-up of a segment).
+//
+// The window sums run on pairs of float32 values with packed instructions
+// (fma.rn.f32x2 and friends): the statistics as (mu1, mu2) and (E[x^2]+E[y^2],
+// E[xy]), the adjoint maps as (g_mu1, g_e) and (g_e12, g_mu2).  The column
+// passes use the window's symmetry (w_k = w_{10-k}): five paired sums, then six
+// multiply-adds, which also halves the length of each dependent chain.
 //
 // Gradient mode has two uses:
 //   training forward: the gradient fields of mean[n] itself (dL = 1) go to the
@@ -33,43 +40,91 @@
 namespace gbssim {
 namespace {
 
-constexpr int NT = kThreads2d;         // threads per CTA = statistic columns per strip
-constexpr int SW = NT;                 // statistic columns held by a strip
-constexpr int GW = SW - 10;            // gradient columns produced by a strip
-constexpr int IW = SW + 10;            // input columns staged per row
-constexpr int IWP = IW + 2;            // padded pitch (multiple of 4 floats)
+constexpr int NT = kThreads2d;         // threads per CTA
+constexpr int SW = NT;                 // forward-only mode: statistic columns per strip
+constexpr int GW = 116;                // gradient mode: gradient columns per strip
+constexpr int SWG = GW + 10;           // gradient mode: statistic columns per strip (<= NT)
+constexpr int GSHIFT = 2;              // gradient strips start at column GW * s - GSHIFT
+constexpr int IWP = 140;               // float pitch of a staged input row (35 x 16 bytes)
 constexpr int STEP = kTaps;            // rows per step = ring length
-constexpr int KH = 8;                  // columns per row-pass work item
-constexpr int NGH = SW / KH;           // row-pass items per row
+constexpr int RP = NT + 1;             // float4 pitch of a row of hb / vb (one pad slot)
+constexpr int RBUF = STEP * RP + 1;    // hb / vb size in float4 (a guard slot at the end)
 constexpr int KA = 8;                  // columns per adjoint row-pass work item
 constexpr int NGA = (GW + KA - 1) / KA;
-constexpr int NBUF = 3;                // input row blocks in flight
+constexpr int GWP = 124;               // float pitch of a staged gradient row
+constexpr int NBUF = 2;                // input row blocks in flight
 
-static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
-static_assert(IWP % 4 == 0, "input pitch must keep float4 alignment");
+static_assert(SWG <= NT, "one thread per statistic column");
+static_assert(IWP % 4 == 0 && IWP >= SW + 10 && IWP >= GW + 20, "input pitch");
+static_assert(GWP % 4 == 0 && GWP >= NGA * KA, "gradient staging pitch");
+static_assert((NGA - 1) * KA + KA + 9 <= NT + 1, "adjoint reads stay within a row + guard");
+static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
+              "gradient strips stage from 16-byte aligned columns");
 
-// Shared-memory layout: xs, ys [NBUF][STEP][IWP] floats, hb [STEP][SW] float4,
-// vb [STEP][SW] float4 (gradient mode only).
+// Staged rows start at input column ic0, a multiple of 4 in both modes (the
+// strips are shifted to make it so): then, when W % 4 == 0 and the images are
+// 16-byte aligned, whole rows move as 16-byte cp.async chunks, entirely inside
+// or entirely outside the image.  Otherwise a 4-byte path stages them.
+__device__ __forceinline__ int stat_shift(int off) { return (4 - (off & 3)) & 3; }
+
+// Shared memory: xs, ys [NBUF][STEP][IWP] floats, hb [RBUF] float4, then in
+// gradient mode vb [RBUF] float4 and sg [1 or 2][STEP][GWP] floats.
+// Work items of the row passes are numbered row-fastest (item = g * STEP + k),
+// so the eight threads of a quarter warp mostly touch eight consecutive rows;
+// with the odd pitches (RP float4 = 129, GWP = 31 float4, IWP = 35 float4) those
+// land in distinct bank groups, and every address inside an item is a base plus
+// a compile-time offset.
 constexpr size_t kInBytes = size_t(2) * NBUF * STEP * IWP * sizeof(float);
-constexpr size_t kRowBytes = size_t(STEP) * SW * sizeof(float4);
+constexpr size_t kRowBytes = size_t(RBUF) * sizeof(float4);
+constexpr size_t kStageBytes = size_t(STEP) * GWP * sizeof(float);
 
-// Column swizzle of hb / vb: writers with a stride of 8 columns and readers with
-// a stride of 1 both hit eight distinct 16-byte bank groups per quarter warp.
-__device__ __forceinline__ int swz(int c) { return (c & ~7) | ((c + (c >> 3)) & 7); }
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
+__device__ __forceinline__ float2 lo(const float4 &v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi(const float4 &v) { return make_float2(v.z, v.w); }
 
-__device__ __forceinline__ float4 f4(float a, float b, float c, float d)
+// sum_a w_a r[(N + 1 + a) % 11] (the oldest entry gets w_0) through the symmetry
+// w_a = w_{10-a}: w_5 r_5 + sum_{a<5} w_a (r_a + r_{10-a}).
+template <int N>
+__device__ __forceinline__ float2 ring_sum2(const float2 (&r)[kTaps])
 {
-    return make_float4(a, b, c, d);
+    float2 acc = __fmul2_rn(splat(tap(5)), r[(N + 6) % kTaps]);
+#pragma unroll
+    for (int a = 0; a < 5; ++a)
+        acc = __ffma2_rn(splat(tap(a)), __fadd2_rn(r[(N + 1 + a) % kTaps], r[(N + 11 - a) % kTaps]),
+                         acc);
+    return acc;
 }
 
-template <bool GRAD, bool G2>
-__global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a)
+template <int N>
+__device__ __forceinline__ float ring_sum1(const float (&r)[kTaps])
 {
+    float acc = tap(5) * r[(N + 6) % kTaps];
+#pragma unroll
+    for (int a = 0; a < 5; ++a)
+        acc = fmaf(tap(a), r[(N + 1 + a) % kTaps] + r[(N + 11 - a) % kTaps], acc);
+    return acc;
+}
+
+// Resident CTAs per SM the kernel is built for: three for the forward-only and
+// the grad_img1 kernels (75 KB of shared memory, <= 168 registers), two with grad_img2.
+template <bool GRAD, bool G2>
+constexpr int min_blocks() { return (GRAD && G2) ? 2 : 3; }
+
+template <bool GRAD, bool G2>
+__global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kernel(const Ssim2dArgs a)
+{
+    constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
+    constexpr int NGH = SW / KH;
+    static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
+
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *xs = reinterpret_cast<float *>(smem_raw);
     float *ys = xs + NBUF * STEP * IWP;
     float4 *hb = reinterpret_cast<float4 *>(smem_raw + kInBytes);
-    float4 *vb = hb + STEP * SW;
+    float4 *vb = hb + RBUF;
+    float *sg1 = reinterpret_cast<float *>(smem_raw + kInBytes + 2 * kRowBytes);
+    float *sg2 = sg1 + STEP * GWP;
     __shared__ double red[NT / 32];
 
     const int tid = threadIdx.x;
@@ -87,7 +142,7 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
     // in gradient mode statistic row p completes gradient row q = p - off = r - 10.
     int j0 = 0, sc0, ic0, R0, nrows, q0 = 0, q1 = 0;
     if (GRAD) {
-        j0 = strip * GW;
+        j0 = strip * GW - GSHIFT;
         q0 = seg * a.seg_rows;
         q1 = min(q0 + a.seg_rows, a.H);
         sc0 = j0 + a.off - 10;
@@ -95,7 +150,7 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
         R0 = q0 - 10;
         nrows = q1 - q0 + 20;
     } else {
-        sc0 = strip * SW;
+        sc0 = strip * SW - stat_shift(a.off);
         const int r0 = seg * a.seg_rows;
         const int r1 = min(r0 + a.seg_rows, a.Ho);
         ic0 = sc0 - a.off;
@@ -105,25 +160,52 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
     const int steps = (nrows + STEP - 1) / STEP;
     const int Rend = R0 + nrows;
 
-    // ---- stage one block of STEP input rows into buffer t % NBUF (zeros outside)
+    // ---- staging of one block of STEP input rows into buffer t % NBUF (zeros outside)
+    constexpr int NCOL = GRAD ? GW + 20 : SW + 10;  // input columns a strip needs
+    constexpr int NCHK = (NCOL + 3) / 4;            // as 16-byte chunks
+    const int cA = ic0 + tid, cB = ic0 + tid + NT;   // 4-byte path: columns tid, tid + NT
+    const bool inA = (cA >= 0) && (cA < a.W);
+    const bool hasB = (tid + NT) < NCOL;
+    const bool inB = hasB && (cB >= 0) && (cB < a.W);
     auto load_block = [&](int t) {
         const int buf = t % NBUF;
         const int rbase = R0 + t * STEP;
-        for (int e = tid; e < STEP * IW; e += NT) {
-            const int ri = e / IW, ci = e - ri * IW;
-            const int R = rbase + ri, Cc = ic0 + ci;
-            const bool inb = (R >= 0) && (R < a.H) && (Cc >= 0) && (Cc < a.W);
-            const size_t gi = inb ? size_t(R) * a.W + Cc : 0;
-            const int si = (buf * STEP + ri) * IWP + ci;
-            cp_async4(xs + si, xp + gi, inb);
-            cp_async4(ys + si, yp + gi, inb);
+        if (a.vec16) {
+            for (int e = tid; e < STEP * NCHK; e += NT) {
+                const int ri = e / NCHK, ch = e - ri * NCHK;
+                const int R = rbase + ri, Cc = ic0 + 4 * ch;
+                const bool inb = (R >= 0) && (R < a.H) && (Cc >= 0) && (Cc < a.W);
+                const size_t gi = inb ? size_t(R) * a.W + Cc : 0;
+                const int si = (buf * STEP + ri) * IWP + 4 * ch;
+                cp_async16(xs + si, xp + gi, inb);
+                cp_async16(ys + si, yp + gi, inb);
+            }
+            return;
+        }
+        float *dx = xs + buf * STEP * IWP + tid;
+        float *dy = ys + buf * STEP * IWP + tid;
+#pragma unroll
+        for (int ri = 0; ri < STEP; ++ri) {
+            const int R = rbase + ri;
+            const bool rin = (R >= 0) && (R < a.H);
+            const size_t roff = rin ? size_t(R) * a.W : 0;
+            const bool okA = rin && inA;
+            const size_t gA = okA ? roff + cA : 0;
+            cp_async4(dx + ri * IWP, xp + gA, okA);
+            cp_async4(dy + ri * IWP, yp + gA, okA);
+            if (hasB) {
+                const bool okB = rin && inB;
+                const size_t gB = okB ? roff + cB : 0;
+                cp_async4(dx + ri * IWP + NT, xp + gB, okB);
+                cp_async4(dy + ri * IWP + NT, yp + gB, okB);
+            }
         }
     };
 
     // ---- row pass of the statistics: row k of block t, columns [KH g, KH g + KH)
     auto h_item = [&](int t, int item) {
-        const int k = item / NGH, g = item - k * NGH;
-        const int base = ((t % NBUF) * STEP + k) * IWP + g * KH;
+        const int g = item / STEP, k = item - g * STEP;
+        const int base = ((t % NBUF) * STEP + k) * IWP + g * KH;  // float4-aligned
         float xv[KH + 10], yv[KH + 10];
 #pragma unroll
         for (int m = 0; m < KH + 8; m += 4) {
@@ -138,93 +220,123 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
             xv[KH + 8] = u.x; xv[KH + 9] = u.y;
             yv[KH + 8] = v.x; yv[KH + 9] = v.y;
         }
-        float acc[KH][4];
+        float2 accA[KH], accB[KH];  // (m1, m2), (es, e12)
 #pragma unroll
         for (int m = 0; m < KH + 10; ++m) {
-            const float x = xv[m] - kShift, y = yv[m] - kShift;
-            const float pe = fmaf(x, x, y * y);
-            const float pc = x * y;
+            const float2 p = f2(xv[m] - kShift, yv[m] - kShift);
+            const float2 sq = __fmul2_rn(p, p);
+            const float2 q = f2(sq.x + sq.y, p.x * p.y);
 #pragma unroll
             for (int o = 0; o < KH; ++o) {
                 const int b = m - o;
                 if (b < 0 || b > 10) continue;
-                const float w = tap(b);
+                const float2 w = splat(tap(b));
                 if (b == 0) {
-                    acc[o][0] = w * x; acc[o][1] = w * y; acc[o][2] = w * pe; acc[o][3] = w * pc;
+                    accA[o] = __fmul2_rn(w, p);
+                    accB[o] = __fmul2_rn(w, q);
                 } else {
-                    acc[o][0] = fmaf(w, x, acc[o][0]);
-                    acc[o][1] = fmaf(w, y, acc[o][1]);
-                    acc[o][2] = fmaf(w, pe, acc[o][2]);
-                    acc[o][3] = fmaf(w, pc, acc[o][3]);
+                    accA[o] = __ffma2_rn(w, p, accA[o]);
+                    accB[o] = __ffma2_rn(w, q, accB[o]);
                 }
             }
         }
+        float4 *dst = hb + k * RP + g * KH;
 #pragma unroll
         for (int o = 0; o < KH; ++o)
-            hb[k * SW + swz(g * KH + o)] = f4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+            dst[o] = make_float4(accA[o].x, accA[o].y, accB[o].x, accB[o].y);
     };
 
     const float scale = (GRAD && a.dL) ? a.dL[n] * a.inv_count : a.inv_count;
 
-    // ---- row pass of the adjoint for gradient row of (block t, row k), chain rule, store
+    // ---- row pass of the adjoint for the gradient row of (block t, row k) and the
+    //      chain rule (input pixels re-read through L1 / L2); results to sg1 / sg2.
     auto a_item = [&](int t, int item) {
-        const int k = item / NGA, g = item - k * NGA;
+        const int g = item / STEP, k = item - g * STEP;
         const int q = R0 + t * STEP + k - 10;
         if (q < q0 || q >= q1) return;
-        // input row q: block t row 0 when k == 10, else block t-1 row k+1
-        const int tq = (k == STEP - 1) ? t : t - 1;
-        const int kq = (k == STEP - 1) ? 0 : k + 1;
-        const int xbase = ((tq % NBUF) * STEP + kq) * IWP + 10;
-        float acc[KA][4];
+        const float4 *src = vb + k * RP + g * KA;
+        // the input pixels of the chain rule, fetched first (through L1 / L2)
+        const size_t rowg = size_t(q) * a.W;
+        float xq[KA], yq[KA];
+#pragma unroll
+        for (int o = 0; o < KA; ++o) {
+            const int jj = g * KA + o, j = j0 + jj;
+            const bool in = (jj < GW) && (j >= 0) && (j < a.W);
+            xq[o] = in ? __ldg(xp + rowg + j) : kShift;
+            yq[o] = in ? __ldg(yp + rowg + j) : kShift;
+        }
+        float2 accA[KA];             // (B^T g_m1, B^T g_e)
+        float2 accB[KA];             // (B^T g_e12, B^T g_m2)   [G2]
+        float accC[KA];              // B^T g_e12              [grad1 only]
 #pragma unroll
         for (int m = 0; m < KA + 10; ++m) {
-            const int c = min(g * KA + m, SW - 1);  // past the strip only for unused outputs
-            const float4 v = vb[k * SW + swz(c)];
+            const float4 v = src[m];  // past the strip (or into the guard) only for unused outputs
 #pragma unroll
             for (int o = 0; o < KA; ++o) {
                 const int b = m - o;
                 if (b < 0 || b > 10) continue;
-                const float w = tap(b);
+                const float2 w = splat(tap(b));
                 if (b == 0) {
-                    acc[o][0] = w * v.x; acc[o][1] = w * v.y; acc[o][2] = w * v.z;
-                    if (G2) acc[o][3] = w * v.w;
+                    accA[o] = __fmul2_rn(w, lo(v));
+                    if (G2) accB[o] = __fmul2_rn(w, hi(v)); else accC[o] = w.x * v.z;
                 } else {
-                    acc[o][0] = fmaf(w, v.x, acc[o][0]);
-                    acc[o][1] = fmaf(w, v.y, acc[o][1]);
-                    acc[o][2] = fmaf(w, v.z, acc[o][2]);
-                    if (G2) acc[o][3] = fmaf(w, v.w, acc[o][3]);
+                    accA[o] = __ffma2_rn(w, lo(v), accA[o]);
+                    if (G2) accB[o] = __ffma2_rn(w, hi(v), accB[o]); else accC[o] = fmaf(w.x, v.z, accC[o]);
                 }
             }
         }
-        float *o1 = a.out1 + plane_off + size_t(q) * a.W;
-        float *o2 = G2 ? a.out2 + plane_off + size_t(q) * a.W : nullptr;
+        float r1[KA], r2[KA];
 #pragma unroll
         for (int o = 0; o < KA; ++o) {
-            const int jj = g * KA + o;
-            const int j = j0 + jj;
-            if (jj < GW && j < a.W) {
-                const float x = xs[xbase + jj] - kShift;
-                const float y = ys[xbase + jj] - kShift;
-                // acc = (B^T g_m1, B^T g_e, B^T g_e12, B^T g_m2)
-                o1[j] = scale * fmaf(2.0f * x, acc[o][1], fmaf(y, acc[o][2], acc[o][0]));
-                if (G2) o2[j] = scale * fmaf(2.0f * y, acc[o][1], fmaf(x, acc[o][2], acc[o][3]));
-            }
+            const float x = xq[o] - kShift, y = yq[o] - kShift;
+            const float e12 = G2 ? accB[o].x : accC[o];
+            r1[o] = scale * fmaf(2.0f * x, accA[o].y, fmaf(y, e12, accA[o].x));
+            if (G2) r2[o] = scale * fmaf(2.0f * y, accA[o].y, fmaf(x, e12, accB[o].y));
+        }
+        float *d1 = sg1 + k * GWP + g * KA;
+#pragma unroll
+        for (int o = 0; o < KA; o += 4)
+            *reinterpret_cast<float4 *>(d1 + o) = make_float4(r1[o], r1[o + 1], r1[o + 2], r1[o + 3]);
+        if (G2) {
+            float *d2 = sg2 + k * GWP + g * KA;
+#pragma unroll
+            for (int o = 0; o < KA; o += 4)
+                *reinterpret_cast<float4 *>(d2 + o) = make_float4(r2[o], r2[o + 1], r2[o + 2], r2[o + 3]);
+        }
+    };
+
+    // ---- store the staged gradient rows of step t (one column per thread)
+    const int jcol = j0 + tid;
+    const bool store_col = GRAD && (tid < GW) && (jcol >= 0) && (jcol < a.W);
+    auto store_rows = [&](int t) {
+        if (!store_col) return;
+        const int qb = R0 + t * STEP - 10;
+#pragma unroll
+        for (int k = 0; k < STEP; ++k) {
+            const int q = qb + k;
+            if (q < q0 || q >= q1) continue;
+            const size_t gi = plane_off + size_t(q) * a.W + jcol;
+            a.out1[gi] = sg1[k * GWP + tid];
+            if (G2) a.out2[gi] = sg2[k * GWP + tid];
         }
     };
 
     // ---- column pass state: registers of thread tid (statistic column sc0 + tid)
-    float4 hr[STEP];
-    float4 gr[STEP];
+    float2 hA[STEP], hB[STEP];   // row-blurred (m1, m2), (es, e12)
+    float2 gA[STEP];             // (g_m1, g_e)
+    float2 gB[STEP];             // (g_e12, g_m2)   [G2]
+    float gC[STEP];              // g_e12           [grad1 only]
 #pragma unroll
     for (int k = 0; k < STEP; ++k) {
-        hr[k] = f4(0.f, 0.f, 0.f, 0.f);
-        gr[k] = f4(0.f, 0.f, 0.f, 0.f);
+        hA[k] = hB[k] = gA[k] = gB[k] = f2(0.f, 0.f);
+        gC[k] = 0.f;
     }
     const int pc = sc0 + tid;
-    const bool col_ok = (pc >= 0) && (pc < a.Wo);
+    const bool col_ok = (tid < (GRAD ? SWG : SW)) && (pc >= 0) && (pc < a.Wo);
     const bool col_own = GRAD ? (tid >= 10 || strip == 0) : true;
     const bool want_mean = (a.partials != nullptr);
     float ssum = 0.0f;
+    int klo = 0, khi = 0, kown = 0;  // rows k of the current step: valid in [klo, khi), owned from kown
 
     // ---- prologue
     load_block(0);
@@ -236,52 +348,64 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
     for (int i = tid; i < STEP * NGH; i += NT) h_item(0, i);
     __syncthreads();
 
-    for (int t = 0; t < steps; ++t) {
-        // ---- V: column passes of step t
-#pragma unroll
-        for (int k = 0; k < STEP; ++k) {
-            hr[k] = hb[k * SW + swz(tid)];
-            Moments mo{0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int aa = 0; aa < STEP; ++aa) {
-                const float4 h = hr[(k + 1 + aa) % STEP];
-                const float w = tap(aa);
-                mo.m1 = fmaf(w, h.x, mo.m1);
-                mo.m2 = fmaf(w, h.y, mo.m2);
-                mo.es = fmaf(w, h.z, mo.es);
-                mo.e12 = fmaf(w, h.w, mo.e12);
+    auto v_row = [&](auto K_, int t) {
+        constexpr int k = decltype(K_)::value;
+        const float4 h = hb[k * RP + tid];
+        hA[k] = lo(h);
+        hB[k] = hi(h);
+        const float2 M = ring_sum2<k>(hA);
+        const float2 E = ring_sum2<k>(hB);
+        const Moments mo{M.x, M.y, E.x, E.y};
+        const bool ok = col_ok && (k >= klo) && (k < khi);
+        const int p = R0 + t * STEP + k + a.off - 10;
+        if (GRAD) {
+            MomentGrads gg;
+            const float S = ssim_and_grads(mo, gg);
+            gA[k] = ok ? f2(gg.g_m1, gg.g_e) : f2(0.f, 0.f);
+            if (G2) gB[k] = ok ? f2(gg.g_e12, gg.g_m2) : f2(0.f, 0.f);
+            else gC[k] = ok ? gg.g_e12 : 0.f;
+            if (want_mean && ok && col_own && k >= kown) {
+                ssum += S;
+                if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
             }
-            const int r = R0 + t * STEP + k;
-            const int p = r + a.off - 10;
-            const bool ok = col_ok && (r >= R0 + 10) && (r < Rend) && (p >= 0) && (p < a.Ho);
-            if (GRAD) {
-                MomentGrads gg;
-                const float S = ssim_and_grads(mo, gg);
-                gr[k] = ok ? f4(gg.g_m1, gg.g_e, gg.g_e12, gg.g_m2) : f4(0.f, 0.f, 0.f, 0.f);
-                const bool own = ok && col_own && (r - 10 >= q0 || seg == 0);
-                if (own) {
-                    ssum += S;
-                    if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
-                }
-                float4 v = f4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int aa = 0; aa < STEP; ++aa) {
-                    const float4 gv = gr[(k + 1 + aa) % STEP];
-                    const float w = tap(aa);
-                    v.x = fmaf(w, gv.x, v.x);
-                    v.y = fmaf(w, gv.y, v.y);
-                    v.z = fmaf(w, gv.z, v.z);
-                    if (G2) v.w = fmaf(w, gv.w, v.w);
-                }
-                vb[k * SW + swz(tid)] = v;
+            const float2 vA = ring_sum2<k>(gA);
+            float4 v;
+            if (G2) {
+                const float2 vB = ring_sum2<k>(gB);
+                v = make_float4(vA.x, vA.y, vB.x, vB.y);
             } else {
-                const float S = ssim_value(mo);
-                if (ok) {
-                    ssum += S;
-                    if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
-                }
+                v = make_float4(vA.x, vA.y, ring_sum1<k>(gC), 0.f);
+            }
+            vb[k * RP + tid] = v;
+        } else {
+            const float S = ssim_value(mo);
+            if (ok) {
+                ssum += S;
+                if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
             }
         }
+    };
+
+    for (int t = 0; t < steps; ++t) {
+        // rows of this step: r = rb + k, statistic row p = r + off - 10
+        const int rb = R0 + t * STEP;
+        const int pb = rb + a.off - 10;
+        klo = max(max(0, R0 + 10 - rb), -pb);
+        khi = min(min(STEP, Rend - rb), a.Ho - pb);
+        kown = (GRAD && seg != 0) ? q0 + 10 - rb : 0;  // q = r - 10 >= q0
+        // ---- V: column passes of step t, and the stores of step t-1's gradient rows
+        if (GRAD && t > 0) store_rows(t - 1);
+        v_row(std::integral_constant<int, 0>{}, t);
+        v_row(std::integral_constant<int, 1>{}, t);
+        v_row(std::integral_constant<int, 2>{}, t);
+        v_row(std::integral_constant<int, 3>{}, t);
+        v_row(std::integral_constant<int, 4>{}, t);
+        v_row(std::integral_constant<int, 5>{}, t);
+        v_row(std::integral_constant<int, 6>{}, t);
+        v_row(std::integral_constant<int, 7>{}, t);
+        v_row(std::integral_constant<int, 8>{}, t);
+        v_row(std::integral_constant<int, 9>{}, t);
+        v_row(std::integral_constant<int, 10>{}, t);
         cp_async_wait<0>();  // block t+1 has landed
         __syncthreads();
         // ---- H of step t+1 and A of step t
@@ -294,10 +418,11 @@ __global__ void __launch_bounds__(NT, 2) ssim2d_stream_kernel(const Ssim2dArgs a
                 a_item(t, i - nh);
         }
         __syncthreads();
-        if (t + 2 < steps) load_block(t + 2);  // into the buffer A(t) just released
+        if (t + 2 < steps) load_block(t + 2);  // into block t's buffer, read by H(t) long ago
         cp_async_commit();
     }
     cp_async_wait<0>();
+    if (GRAD) store_rows(steps - 1);  // the last staged rows (the final barrier above orders them)
 
     if (want_mean) {
         const double tot = block_sum<NT>(ssum, red);
@@ -342,20 +467,28 @@ __global__ void __launch_bounds__(256) scale_fields_scalar(const float *f1, cons
     }
 }
 
+size_t smem_bytes(bool grad, bool g2)
+{
+    return kInBytes + (grad ? 2 * kRowBytes + (g2 ? 2 : 1) * kStageBytes : kRowBytes);
+}
+
 template <bool GRAD, bool G2>
 cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
 {
-    const size_t smem = kInBytes + (GRAD ? 2 : 1) * kRowBytes;
-    ssim2d_stream_kernel<GRAD, G2><<<blocks, NT, smem, s>>>(a);
+    ssim2d_stream_kernel<GRAD, G2><<<blocks, NT, smem_bytes(GRAD, G2), s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t ssim2d_smem_bytes(bool grad) { return kInBytes + (grad ? 2 : 1) * kRowBytes; }
+size_t ssim2d_smem_bytes(bool grad, bool g2) { return smem_bytes(grad, g2); }
 
-int ssim2d_grad_cols() { return GW; }
-int ssim2d_stat_cols() { return SW; }
+int ssim2d_strips(bool grad, int W, int Wo, int off)
+{
+    if (grad) return (W + GSHIFT + GW - 1) / GW;
+    const int shift = (4 - (off & 3)) & 3;
+    return (Wo + shift + SW - 1) / SW;
+}
 
 const void *ssim2d_kernel_ptr(bool grad, bool g2)
 {

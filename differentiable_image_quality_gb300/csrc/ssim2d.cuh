@@ -18,6 +18,7 @@ struct Ssim2dArgs {
     int off;         // window offset: 0 valid, 5 same
     int C;           // channels (plane / C = image index)
     int strips, segs, seg_rows;
+    int vec16;       // 1: W % 4 == 0 and x, y 16-byte aligned (16-byte staging)
     // gradient mode: fields written here (grad of mean[n] * dL[n]); out2 may be null
     float *out1, *out2;
     const float *dL;  // [N] or null (then dL = 1)
@@ -31,9 +32,9 @@ struct Ssim2dArgs {
     double count;
 };
 
-size_t ssim2d_smem_bytes(bool grad);
-int ssim2d_grad_cols();  // gradient columns per strip
-int ssim2d_stat_cols();  // statistic columns per strip (forward-only mode)
+size_t ssim2d_smem_bytes(bool grad, bool g2);
+// Column strips of a plane in gradient mode (over W) or forward-only mode (over Wo).
+int ssim2d_strips(bool grad, int W, int Wo, int off);
 const void *ssim2d_kernel_ptr(bool grad, bool g2);
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s);
 

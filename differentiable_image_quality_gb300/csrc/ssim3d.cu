@@ -40,15 +40,6 @@ constexpr size_t kYBytes = size_t(TY) * TX * sizeof(float4);
 
 __device__ __forceinline__ int swz(int c) { return (c & ~7) | ((c + (c >> 3)) & 7); }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool in_bounds)
-{
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    const int src_bytes = in_bounds ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ float4 wsum_ring(const float4 (&ring)[kTaps], int newest)
 {
     // sum_a w_a ring[(newest + 1 + a) % 11]: the oldest slice gets w_0

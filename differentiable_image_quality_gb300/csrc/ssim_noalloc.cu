@@ -14,7 +14,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/gbssim.h"
+#include "gbssim.h"
 
 namespace {
 

@@ -286,3 +286,37 @@ def test_python_api_errors(dev):
         pkg.fused_ssim(a.transpose(2, 3), a)
     with pytest.raises(pkg.GbssimError):
         pkg.fused_ssim(a[:, :, :10], a[:, :, :10].clone(), padding="valid")
+
+
+@pytest.mark.parametrize("padding", ["valid", "same"])
+def test_parity_unaligned_base_pointers(dev, oracle_mod, padding):
+    """Images that start 4 bytes past a 16-byte boundary (W % 4 == 0): the
+    4-byte staging path instead of the 16-byte one."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    shape = (1, 2, 40, 260)
+    x, y = uniform_pair(shape, 704, std=0.1)
+    n = int(np.prod(shape))
+    bx = torch.empty(n + 1, device=dev)
+    by = torch.empty(n + 1, device=dev)
+    tx = bx[1:].view(shape)
+    ty = by[1:].view(shape)
+    tx.copy_(torch.from_numpy(x))
+    ty.copy_(torch.from_numpy(y))
+    assert tx.data_ptr() % 16 == 4
+    mean = torch.empty(1, device=dev)
+    saved = torch.empty(pkg.saved_bytes(shape, True) // 4, device=dev)
+    pkg.ssim_fwd(tx, ty, padding, mean, saved=saved, want_grad2=True)
+    g1, g2 = torch.empty_like(tx), torch.empty_like(ty)
+    r1 = torch.empty_like(tx)
+    dl = torch.tensor([-1.0], device=dev)
+    pkg.ssim_bwd(dl, tx, ty, padding, g1, g2, saved=saved)
+    pkg.ssim_bwd(dl, tx, ty, padding, r1)
+    torch.cuda.synchronize()
+    ref = _oracle(oracle_mod, x, y, [-1.0], padding, True)
+    _assert_parity({"mean": mean.cpu().numpy(), "g1": g1.cpu().numpy(), "g2": g2.cpu().numpy()},
+                   ref, True, f"unaligned {padding}")
+    _assert_parity({"mean": mean.cpu().numpy(), "g1": r1.cpu().numpy()}, ref, False,
+                   f"unaligned recompute {padding}")
