@@ -47,6 +47,10 @@ PROFILE = os.path.join(ROOT, "profiles", "ssim2d_grad_splat1080_valid.md")
 GRAD_FMA_PER_PIXEL = 44 + 44 + 33 + 33  # row + column passes of 4 statistics, of 3 adjoint maps
 GRAD_OTHER_PER_PIXEL = 5 + 30 + 3       # shifted products, SSIM and derivatives, chain rule
 GRAD_FLOPS_PER_PIXEL = 2 * GRAD_FMA_PER_PIXEL + GRAD_OTHER_PER_PIXEL
+# 3D (statistics and adjoint kernels together): three 11-tap passes of four
+# statistics and of three adjoint maps, plus the same per-voxel work.
+GRAD3D_FLOPS_PER_VOXEL = 2 * (3 * 44 + 3 * 33) + GRAD_OTHER_PER_PIXEL
+KERNEL3D_NAME = "ssim3d_stats_kernel<true> + ssim3d_adjoint_kernel<false>"
 
 
 def parse():
@@ -57,6 +61,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the extra timed variants")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name from workloads.WORKLOADS (default: the 1080p valid pair)")
     return ap.parse_args()
 
 
@@ -138,45 +144,65 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle (CPU)
 
-def oracle_band(n_rows: int):
-    """(x, y, dl) for the first n_rows rows of the workload pair (a bounded sample)."""
+def oracle_band(name: str, n_rows: int):
+    """(x, y, dl) for the first n_rows rows (2D) or slices (3D) of the workload
+    pair: a bounded sample of it."""
     from workloads import dl_vector, make_inputs
 
-    x, y = make_inputs(WORKLOAD)
+    x, y = make_inputs(name)
     n_rows = max(11, min(n_rows, x.shape[2]))
-    return (x[:, :, :n_rows].copy(), y[:, :, :n_rows].copy(), dl_vector(WORKLOAD))
+    return (x[:, :, :n_rows].copy(), y[:, :, :n_rows].copy(), dl_vector(name))
 
 
-def time_oracle_step(oracle, x, y, dl):
+def time_oracle_step(oracle, x, y, dl, padding="valid", want_grad2=False):
     t0 = time.perf_counter()
-    oracle.ssim2d(x, y, "valid")
-    oracle.ssim2d_grad(x, y, dl, "valid", want_grad2=False)
+    if x.ndim == 5:
+        oracle.ssim3d(x, y, padding)
+        oracle.ssim3d_grad(x, y, dl, padding, want_grad2=want_grad2)
+    else:
+        oracle.ssim2d(x, y, padding)
+        oracle.ssim2d_grad(x, y, dl, padding, want_grad2=want_grad2)
     return time.perf_counter() - t0
 
 
-def size_oracle_band(oracle, target_s: float):
-    """Rows of the 1080p pair whose oracle step takes about target_s seconds."""
-    rows = 32
-    x, y, dl = oracle_band(rows)
-    t = time_oracle_step(oracle, x, y, dl)
-    while t < target_s / 2 and rows < 1080:
-        rows = min(1080, int(rows * min(8.0, max(2.0, target_s / max(t, 1e-3)))))
-        x, y, dl = oracle_band(rows)
-        t = time_oracle_step(oracle, x, y, dl)
+def size_oracle_band(oracle, name, target_s: float):
+    """Rows (slices) of the workload whose oracle step takes about target_s seconds."""
+    from workloads import WORKLOADS
+
+    wl = WORKLOADS[name]
+    full = wl.shape[2]
+    rows = 32 if wl.ndim == 2 else 12
+    x, y, dl = oracle_band(name, rows)
+    t = time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2)
+    while t < target_s / 2 and rows < full:
+        rows = min(full, int(rows * min(8.0, max(2.0, target_s / max(t, 1e-3)))))
+        x, y, dl = oracle_band(name, rows)
+        t = time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2)
     return rows, (x, y, dl), t
 
 
-def cpu_baseline(target_s: float = 4.0):
-    import oracle
+def units(shape):
+    """Megapixels (megavoxels) per step: N times the spatial extent, channels not counted."""
+    n = shape[0]
+    for s in shape[2:]:
+        n *= s
+    return n / 1e6
 
+
+def cpu_baseline(name: str, unit: str, target_s: float = 4.0):
+    import oracle
+    from workloads import WORKLOADS
+
+    wl = WORKLOADS[name]
     oracle.build()
-    rows, (x, y, dl), _ = size_oracle_band(oracle, target_s)
-    times = [time_oracle_step(oracle, x, y, dl) for _ in range(3)]
+    rows, (x, y, dl), _ = size_oracle_band(oracle, name, target_s)
+    times = [time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2) for _ in range(3)]
     t = statistics.median(times)
-    mp = x.shape[0] * x.shape[2] * x.shape[3] / 1e6
-    return {"value": mp / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"rows 0..{rows} of the 1x3x1080x1920 pair (valid), mean + grad_img1, "
-                      f"median of 3 ({t:.2f} s each)"}
+    what = "rows" if wl.ndim == 2 else "slices"
+    return {"value": units(x.shape) / t, "unit": unit, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{what} 0..{rows} of the {'x'.join(map(str, wl.shape))} pair ({wl.padding}), "
+                      f"mean + gradients, median of 3 ({t:.2f} s each)"}
 
 
 def run_reference(args):
@@ -184,28 +210,34 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
+    from workloads import WORKLOADS
 
+    wl = WORKLOADS[args.workload]
+    unit = UNIT if wl.ndim == 2 else "Mvoxel/s"
     oracle.build()
     budget = 150.0  # seconds for the whole run
     per_step = max(0.5, min(5.0, budget / max(1, args.steps + args.warmup)))
-    rows, (x, y, dl), _ = size_oracle_band(oracle, per_step)
+    rows, (x, y, dl), _ = size_oracle_band(oracle, args.workload, per_step)
     for _ in range(args.warmup):
-        time_oracle_step(oracle, x, y, dl)
-    times = [time_oracle_step(oracle, x, y, dl) for _ in range(args.steps)]
-    mp = x.shape[0] * x.shape[2] * x.shape[3] / 1e6
+        time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2)
+    times = [time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2)
+             for _ in range(args.steps)]
+    mp = units(x.shape)
     total = sum(times)
     value = mp * len(times) / total
+    what = "rows" if wl.ndim == 2 else "slices"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "shape": [1, 3, 1080, 1920], "padding": "valid",
-                   "grads": "img1", "sample_rows": rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+        "config": {"workload": args.workload, "shape": list(wl.shape), "padding": wl.padding,
+                   "grads": "img1, img2" if wl.want_grad2 else "img1", "sample_" + what: rows},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"rows 0..{rows} of the 1x3x1080x1920 pair per step"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                         "sample": f"{what} 0..{rows} of the {'x'.join(map(str, wl.shape))} "
+                                   f"pair per step"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -236,7 +268,6 @@ def profiled_traffic():
 
 
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -249,23 +280,28 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg._abi.load()
-    wl = WORKLOADS[WORKLOAD]
-    x, y = make_inputs(WORKLOAD)
-    dl = dl_vector(WORKLOAD)
-    N, C, H, W = x.shape
-    mp = N * H * W / 1e6
+    name = args.workload
+    wl = WORKLOADS[name]
+    is3d = wl.ndim == 3
+    unit = UNIT if not is3d else "Mvoxel/s"
+    x, y = make_inputs(name)
+    dl = dl_vector(name)
+    N, C = x.shape[:2]
+    elems = x.size
+    mp = units(x.shape)
+    g2wanted = wl.want_grad2
+    fwd_call = pkg.ssim3d_fwd if is3d else pkg.ssim_fwd
+    bwd_call = pkg.ssim3d_bwd if is3d else pkg.ssim_bwd
+    fused_call = pkg.ssim3d_fwd_bwd if is3d else pkg.ssim_fwd_bwd
 
     tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
     tdl = torch.from_numpy(dl).to(dev)
     mean = torch.empty(N, device=dev)
-    saved = torch.empty(pkg.saved_bytes(x.shape, False) // 4, device=dev)
+    saved = torch.empty(pkg.saved_bytes(x.shape, g2wanted) // 4, device=dev)
     g1 = torch.empty_like(tx)
+    g2 = torch.empty_like(ty) if g2wanted else None
     flush = torch.empty(FLUSH_BYTES // 4, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step_saved():
-        pkg.ssim_fwd(tx, ty, wl.padding, mean, saved=saved, want_grad2=False)
-        pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1, saved=saved)
 
     def timed(fn_a, fn_b, steps, warmup):
         """Per-step device times of fn_a then fn_b, L2 flushed before each step."""
@@ -296,10 +332,10 @@ def run_ours(args):
         return ta, tb
 
     def fwd_train():
-        pkg.ssim_fwd(tx, ty, wl.padding, mean, saved=saved, want_grad2=False)
+        fwd_call(tx, ty, wl.padding, mean, saved=saved, want_grad2=g2wanted)
 
     def bwd_saved():
-        pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1, saved=saved)
+        bwd_call(tdl, tx, ty, wl.padding, g1, g2, saved=saved)
 
     with ClockSampler(local) as clocks:
         ta, tb = timed(fwd_train, bwd_saved, args.steps, max(3, args.warmup))
@@ -318,16 +354,19 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers (pinned)
     hx = torch.from_numpy(x).pin_memory()
     hy = torch.from_numpy(y).pin_memory()
-    hg = torch.empty(x.shape, dtype=torch.float32).pin_memory()
+    hg1 = torch.empty(x.shape, dtype=torch.float32).pin_memory()
+    hg2 = torch.empty(x.shape, dtype=torch.float32).pin_memory() if g2wanted else None
     hm = torch.empty(N, dtype=torch.float32).pin_memory()
     dx, dy = torch.empty_like(tx), torch.empty_like(ty)
 
     def e2e_step():
         dx.copy_(hx, non_blocking=True)
         dy.copy_(hy, non_blocking=True)
-        pkg.ssim_fwd(dx, dy, wl.padding, mean, saved=saved, want_grad2=False)
-        pkg.ssim_bwd(tdl, dx, dy, wl.padding, g1, saved=saved)
-        hg.copy_(g1, non_blocking=True)
+        fwd_call(dx, dy, wl.padding, mean, saved=saved, want_grad2=g2wanted)
+        bwd_call(tdl, dx, dy, wl.padding, g1, g2, saved=saved)
+        hg1.copy_(g1, non_blocking=True)
+        if g2wanted:
+            hg2.copy_(g2, non_blocking=True)
         hm.copy_(mean, non_blocking=True)
 
     te, _ = timed(e2e_step, None, args.steps, max(3, args.warmup))
@@ -340,20 +379,24 @@ def run_ours(args):
 
     extras = {}
     if not args.no_extras:
-        # recompute backward (no saved fields) and the inference forward
         def fwd_infer():
-            pkg.ssim_fwd(tx, ty, wl.padding, mean)
+            fwd_call(tx, ty, wl.padding, mean)
 
         def bwd_recompute():
-            pkg.ssim_bwd(tdl, tx, ty, wl.padding, g1)
+            bwd_call(tdl, tx, ty, wl.padding, g1, g2)
+
+        def single_call():
+            fused_call(tx, ty, wl.padding, tdl, mean, g1, g2)
 
         ra, rb = timed(fwd_infer, bwd_recompute, args.steps, 3)
+        sa, _ = timed(single_call, None, args.steps, 3)
         extras = {
             "fwd_train_mps": mp / (fwd_ms / 1e3),
             "bwd_saved_mps": mp / (bwd_ms / 1e3),
             "fwd_infer_mps": mp / (statistics.mean(ra) / 1e3),
             "bwd_recompute_mps": mp / (statistics.mean(rb) / 1e3),
             "recompute_path_fwd_bwd_mps": mp / ((statistics.mean(ra) + statistics.mean(rb)) / 1e3),
+            "single_call_fwd_bwd_mps": mp / (statistics.mean(sa) / 1e3),
         }
 
     if rank != 0:
@@ -366,40 +409,42 @@ def run_ours(args):
     sm_count = props.multi_processor_count
     sm_max = float(clk.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0))
     alu_peak_tflops = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
-    grad_flops = GRAD_FLOPS_PER_PIXEL * N * C * H * W
-    achieved_tflops = grad_flops / (fwd_ms / 1e3) / 1e12
-    min_bytes = (2 * N * C * H * W + 2 * N * C * H * W + N * C * H * W) * 4  # fwd 2 reads; bwd 2 reads + 1 write
+    flops_px = GRAD_FLOPS_PER_PIXEL if not is3d else GRAD3D_FLOPS_PER_VOXEL
+    achieved_tflops = flops_px * elems / (fwd_ms / 1e3) / 1e12
+    grads = 2 if g2wanted else 1
+    min_bytes = (2 * elems + 2 * elems + grads * elems) * 4  # fwd: read 2; bwd: read 2, write grads
     step_s = statistics.mean(step_ms) / 1e3
     hbm_gbs = min_bytes / step_s / 1e9
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline()
+        cpu = cpu_baseline(name, unit)
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "shape": [N, C, H, W], "padding": wl.padding,
-                   "grads": "img1", "path": "saved gradient fields (training forward) + scaling backward",
+        "config": {"workload": name, "shape": list(x.shape), "padding": wl.padding,
+                   "grads": "img1, img2" if g2wanted else "img1",
+                   "path": "saved gradient fields (training forward) + scaling backward",
                    "l2": "flushed before every step (256 MiB write outside the timed events)",
                    "timing": "CUDA events per step on the launching stream; value = K steps / sum"},
-        "gpu_launches": 2 * args.steps,
-        "roofline": {"kernel": KERNEL_NAME, "bound": "alu", "achieved": achieved_tflops,
-                     "peak": alu_peak_tflops, "unit": "TFLOP/s",
+        "gpu_launches": (2 if not is3d else 3) * args.steps,
+        "roofline": {"kernel": KERNEL_NAME if not is3d else KERNEL3D_NAME, "bound": "alu",
+                     "achieved": achieved_tflops, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved_tflops / alu_peak_tflops,
-                     "traffic": profiled_traffic(),
+                     "traffic": profiled_traffic() if (name == WORKLOAD) else None,
                      "peak_basis": f"{sm_count} SMs x 128 fp32 lanes x 2 flops x {sm_max:.0f} MHz",
-                     "flops_per_pixel": GRAD_FLOPS_PER_PIXEL},
+                     "flops_per_pixel": flops_px},
         "hbm_roofline": {"min_bytes_per_step": min_bytes, "achieved_gbs": hbm_gbs,
                          "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
                          "frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
                          "measured_peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": 2 * N * C * H * W * 4,
-                "d2h_bytes_per_step": N * C * H * W * 4 + N * 4},
+        "e2e": {"value": e2e_value, "unit": unit,
+                "h2d_bytes_per_step": 2 * elems * 4,
+                "d2h_bytes_per_step": grads * elems * 4 + N * 4},
         "clocks": clk,
         "cpu_baseline": cpu,
         **extras,

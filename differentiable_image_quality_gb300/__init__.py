@@ -35,6 +35,8 @@ __all__ = [
     "ssim_bwd",
     "ssim3d_fwd",
     "ssim3d_bwd",
+    "ssim_fwd_bwd",
+    "ssim3d_fwd_bwd",
     "workspace_bytes",
     "saved_bytes",
     "window",
@@ -170,6 +172,39 @@ def ssim3d_bwd(dL, img1, img2, padding, grad1, grad2=None, saved=None, workspace
                         0 if workspace is None else workspace.numel() * workspace.element_size(),
                         _stream(img1))
     _abi.check("ssim3d_bwd", st)
+
+
+def ssim_fwd_bwd(img1, img2, padding, dL, out_mean, grad1, grad2=None, out_map=None,
+                 workspace=None):
+    """Forward and backward in one call (dL = dLoss/dmean[n] known beforehand)."""
+    _check_pair(img1, img2, 2)
+    N, C, H, W = img1.shape
+    pad = _pad(padding)
+    lib = _abi.load()
+    if workspace is None:
+        workspace = _workspace(img1.device, int(lib.gbssim_workspace_bytes(N, C, H, W, pad)))
+    st = lib.ssim_fwd_bwd(_abi.ptr(img1), _abi.ptr(img2), N, C, H, W, pad, _abi.ptr(dL),
+                          _abi.ptr(out_mean), _abi.ptr(out_map), _abi.ptr(grad1), _abi.ptr(grad2),
+                          _abi.ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(img1))
+    _abi.check("ssim_fwd_bwd", st)
+
+
+def ssim3d_fwd_bwd(img1, img2, padding, dL, out_mean, grad1, grad2=None, out_map=None,
+                   workspace=None):
+    """ssim_fwd_bwd for NCDHW volumes."""
+    _check_pair(img1, img2, 3)
+    N, C, D, H, W = img1.shape
+    pad = _pad(padding)
+    lib = _abi.load()
+    if workspace is None:
+        workspace = _workspace(img1.device,
+                               int(lib.gbssim3d_workspace_bytes(N, C, D, H, W, pad)))
+    st = lib.ssim3d_fwd_bwd(_abi.ptr(img1), _abi.ptr(img2), N, C, D, H, W, pad, _abi.ptr(dL),
+                            _abi.ptr(out_mean), _abi.ptr(out_map), _abi.ptr(grad1),
+                            _abi.ptr(grad2), _abi.ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(img1))
+    _abi.check("ssim3d_fwd_bwd", st)
 
 
 # ----------------------------------------------------------------- autograd

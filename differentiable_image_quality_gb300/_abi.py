@@ -29,6 +29,9 @@ SIGNATURES = {
     "ssim_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),
     "ssim_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp]),
     "ssim_fwd_noalloc": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp]),
+    "ssim_fwd_bwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]),
+    "ssim3d_fwd_bwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _fp, _fp, _vp, _sz,
+                            _vp]),
     "gbssim3d_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gbssim3d_saved_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "ssim3d_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),

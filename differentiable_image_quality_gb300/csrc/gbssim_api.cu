@@ -555,4 +555,112 @@ int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int
     return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pb.blocks), s));
 }
 
+
+int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+                 const float *dL, float *out_mean, float *out_map_or_null, float *grad_img1,
+                 float *grad_img2_or_null, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(dL)) ||
+        (rc = check_in(out_mean)) || (rc = check_opt(out_map_or_null)) ||
+        (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape2d_ok(N, C, H, W, padding)) return GBSSIM_ESHAPE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return GBSSIM_EWORKSPACE;
+    const size_t img_bytes = size_t(N) * C * H * W * sizeof(float);
+    const bool g2 = grad_img2_or_null != nullptr;
+    const int Ho = out_extent(H, padding), Wo = out_extent(W, padding);
+    const size_t map_bytes = size_t(N) * C * Ho * Wo * sizeof(float);
+    if (overlaps(grad_img1, img_bytes, img1, img_bytes) ||
+        overlaps(grad_img1, img_bytes, img2, img_bytes) ||
+        overlaps(grad_img1, img_bytes, out_map_or_null, map_bytes) ||
+        overlaps(grad_img1, img_bytes, dL, size_t(N) * sizeof(float)) ||
+        (g2 && (overlaps(grad_img2_or_null, img_bytes, img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, img2, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, grad_img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, out_map_or_null, map_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, dL, size_t(N) * sizeof(float)))))
+        return GBSSIM_EINVAL;
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
+                            d->occ2d[g2 ? 2 : 1]);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
+        return GBSSIM_EWORKSPACE;
+    Ssim2dArgs a{};
+    a.x = img1; a.y = img2;
+    a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
+    a.off = off;
+    a.C = C;
+    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    a.out1 = grad_img1;
+    a.out2 = grad_img2_or_null;
+    a.dL = dL;
+    a.inv_count = float(1.0 / (double(C) * double(Ho) * double(Wo)));
+    a.map = out_map_or_null;
+    a.counter = static_cast<unsigned *>(workspace);
+    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
+    a.mean = out_mean;
+    a.images = N;
+    a.blocks_per_image = int(p.blocks / N);
+    a.count = double(C) * double(Ho) * double(Wo);
+    return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), static_cast<cudaStream_t>(stream)));
+}
+
+int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
+                   int padding, const float *dL, float *out_mean, float *out_map_or_null,
+                   float *grad_img1, float *grad_img2_or_null, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(dL)) ||
+        (rc = check_in(out_mean)) || (rc = check_opt(out_map_or_null)) ||
+        (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape3d_ok(N, C, D, H, W, padding)) return GBSSIM_ESHAPE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+        workspace_bytes < gbssim3d_workspace_bytes(N, C, D, H, W, padding))
+        return GBSSIM_EWORKSPACE;
+    const size_t img_bytes = size_t(N) * C * D * H * W * sizeof(float);
+    const bool g2 = grad_img2_or_null != nullptr;
+    if (overlaps(grad_img1, img_bytes, img1, img_bytes) ||
+        overlaps(grad_img1, img_bytes, img2, img_bytes) ||
+        overlaps(grad_img1, img_bytes, workspace, workspace_bytes) ||
+        overlaps(grad_img1, img_bytes, dL, size_t(N) * sizeof(float)) ||
+        (g2 && (overlaps(grad_img2_or_null, img_bytes, img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, img2, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, grad_img1, img_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, workspace, workspace_bytes) ||
+                overlaps(grad_img2_or_null, img_bytes, dL, size_t(N) * sizeof(float)))))
+        return GBSSIM_EINVAL;
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Ssim3dArgs a{};
+    fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    apply_plan(a, pa);
+    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
+    a.mean = out_mean;
+    a.map = out_map_or_null;
+    a.blocks_per_image = int(pa.blocks / N);
+    cudaError_t e = ssim3d_stats_launch(a, true, int(pa.blocks), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    apply_plan(a, pb);
+    a.out1 = grad_img1;
+    a.out2 = grad_img2_or_null;
+    a.dL = dL;
+    return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pb.blocks), s));
+}
+
 }  // extern "C"

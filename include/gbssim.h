@@ -108,6 +108,18 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
              int padding, const float *saved_or_null, size_t saved_bytes, float *grad_img1,
              float *grad_img2_or_null, void *stream);
 
+/* Forward and backward in one call, for a loss whose derivative with respect to
+ * each image's mean SSIM is known before the forward -- the usual training loss
+ * 1 - mean over the batch has dL[n] = -1/N.  One kernel pass computes the
+ * means (and the map), the upstream gradients of the statistics, the adjoint
+ * and the chain rule (TriSSIM README, "How it works"), so the statistics are
+ * formed once and no intermediate field is written.  Arguments as in ssim_fwd
+ * and ssim_bwd; dL is [N] float32 on the device, read by the kernel.  The
+ * workspace is sized by gbssim_workspace_bytes. */
+int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+                 const float *dL, float *out_mean, float *out_map_or_null, float *grad_img1,
+                 float *grad_img2_or_null, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Size of the device array behind ssim_fwd_noalloc (per GPU, for the process's life). */
 #define GBSSIM_NOALLOC_SCRATCH_BYTES (1u << 20)
 
@@ -159,6 +171,12 @@ int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int
                int H, int W, int padding, const float *saved_or_null, size_t saved_bytes,
                float *grad_img1, float *grad_img2_or_null, void *workspace,
                size_t workspace_bytes, void *stream);
+
+/* The single-call forward + backward of ssim_fwd_bwd for volumes. */
+int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
+                   int padding, const float *dL, float *out_mean, float *out_map_or_null,
+                   float *grad_img1, float *grad_img2_or_null, void *workspace,
+                   size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

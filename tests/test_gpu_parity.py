@@ -3,8 +3,11 @@
 Every call goes through the C ABI (via the thin torch wrappers).  Bars, from
 the loss's specification: |mean_gpu - mean_oracle| <= 1e-5 for every image;
 max |grad_gpu - grad_oracle| <= 1e-4 * max |grad_oracle| for each gradient.
-The SSIM map has no stated bar; it is held to 2e-5 absolute (float32 window
-sums of values in [0, 1] carry ~1e-6 absolute error into S).
+The SSIM map has no stated bar; it is held to 2e-4 absolute, from the float32
+error of the window sums: E[x'^2] + E[y'^2] (shifted values, at most 0.5)
+summed over 11 + 11 taps carries ~1e-7 absolute rounding error, and S divides
+the variances by sigma11 + sigma22 + C2, which in flat regions is ~C2 = 9e-4:
+|dS| ~ 1e-7 / 9e-4 ~ 1e-4.  (Textured images stay near 1e-6.)
 """
 import numpy as np
 import pytest
@@ -15,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
 GRAD_RTOL = 1e-4
-MAP_TOL = 2e-5
+MAP_TOL = 2e-4
 
 
 @pytest.fixture(scope="module")
@@ -320,3 +323,32 @@ def test_parity_unaligned_base_pointers(dev, oracle_mod, padding):
                    ref, True, f"unaligned {padding}")
     _assert_parity({"mean": mean.cpu().numpy(), "g1": r1.cpu().numpy()}, ref, False,
                    f"unaligned recompute {padding}")
+
+
+@pytest.mark.parametrize("name", ["tiny64_valid", "splat1080_same", "batch512_valid",
+                                  "volume128_valid"])
+def test_single_call_forward_backward(dev, oracle_mod, name):
+    """ssim_fwd_bwd / ssim3d_fwd_bwd: means, map and gradients from one call."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    wl = WORKLOADS[name]
+    x, y = make_inputs(name)
+    dl = dl_vector(name)
+    tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+    tdl = torch.from_numpy(dl).to(dev)
+    N = x.shape[0]
+    mean = torch.full((N,), float("nan"), device=dev)
+    g1 = torch.full_like(tx, float("nan"))
+    g2 = torch.full_like(ty, float("nan")) if wl.want_grad2 else None
+    ext = [s - 10 if wl.padding == "valid" else s for s in x.shape[2:]]
+    smap = torch.full((N, x.shape[1], *ext), float("nan"), device=dev)
+    call = pkg.ssim3d_fwd_bwd if x.ndim == 5 else pkg.ssim_fwd_bwd
+    call(tx, ty, wl.padding, tdl, mean, g1, g2, out_map=smap)
+    torch.cuda.synchronize()
+    got = {"mean": mean.cpu().numpy(), "g1": g1.cpu().numpy(), "map": smap.cpu().numpy()}
+    if wl.want_grad2:
+        got["g2"] = g2.cpu().numpy()
+    ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2, want_map=True)
+    _assert_parity(got, ref, wl.want_grad2, f"single call {name}")
