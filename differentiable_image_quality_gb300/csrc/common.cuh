@@ -98,41 +98,51 @@ struct MomentGrads {
 //   B2 = sigma_sum + C2.
 __device__ __forceinline__ float ssim_value(const Moments &m)
 {
-    const float mu1 = m.m1 + kShift, mu2 = m.m2 + kShift;
-    const float ss = m.es - m.m1 * m.m1 - m.m2 * m.m2;
-    const float s12 = m.e12 - m.m1 * m.m2;
-    const float A1 = 2.0f * mu1 * mu2 + kC1;
-    const float A2 = 2.0f * s12 + kC2;
-    const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
+    const float2 M = make_float2(m.m1, m.m2);
+    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 msq = __fmul2_rn(M, M);
+    const float2 musq = __fmul2_rn(mu, mu);
+    const float ss = m.es - (msq.x + msq.y);
+    const float s12 = fmaf(-m.m1, m.m2, m.e12);
+    const float B1 = (musq.x + musq.y) + kC1;
     const float B2 = ss + kC2;
-    return A1 * A2 * rcp_approx(B1 * B2);
+    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
+    const float A2 = fmaf(2.0f, s12, kC2);
+    return (A1 * A2) * rcp_approx(B1 * B2);
 }
 
-// S and its derivatives with respect to the shifted moments.
-//   dS/dsigma_sum = -S / B2,  dS/dsigma12 = 2 A1 / (B1 B2),
-//   dS/dmu1 (sigmas fixed) = 2 (mu2 A2 - mu1 S B2) / (B1 B2),
+// S and its derivatives with respect to the shifted moments, written as
+// S = l * cs with l = A1 / B1 (luminance) and cs = A2 / B2 (contrast-structure):
+//   dS/dsigma_sum = -cs * l / B2,   dS/dsigma12 = 2 l / B2,
+//   dS/dmu1 (sigmas fixed) = 2 cs (mu2 - mu1 l) / B1,
 // and through sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2:
-//   dS/dm1 = dS/dmu1 - 2 m1 dS/dsigma_sum - m2 dS/dsigma12   (m2 likewise).
-__device__ __forceinline__ float ssim_and_grads(const Moments &m, MomentGrads &g)
+//   dS/dm1 = dS/dmu1 - 2 m1 dS/dsigma_sum - m2 dS/dsigma12
+//          = 2 cs (mu2 - mu1 l) / B1 + (2 l / B2) (m1 cs - m2)        (m2 likewise).
+// When `valid` is false every derivative (and S) comes out as exactly zero:
+// l and cs are zeroed before they are used.
+template <bool WANT_G2>
+__device__ __forceinline__ float ssim_and_grads(const Moments &m, bool valid, MomentGrads &g)
 {
-    const float mu1 = m.m1 + kShift, mu2 = m.m2 + kShift;
-    const float ss = m.es - m.m1 * m.m1 - m.m2 * m.m2;
-    const float s12 = m.e12 - m.m1 * m.m2;
-    const float A1 = 2.0f * mu1 * mu2 + kC1;
-    const float A2 = 2.0f * s12 + kC2;
-    const float B1 = mu1 * mu1 + mu2 * mu2 + kC1;
+    const float2 M = make_float2(m.m1, m.m2);
+    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 msq = __fmul2_rn(M, M);
+    const float2 musq = __fmul2_rn(mu, mu);
+    const float ss = m.es - (msq.x + msq.y);
+    const float s12 = fmaf(-m.m1, m.m2, m.e12);
+    const float B1 = (musq.x + musq.y) + kC1;
     const float B2 = ss + kC2;
-    const float inv = rcp_approx(B1 * B2);
-    const float S = A1 * A2 * inv;
-    const float d_ss = -S * B1 * inv;      // -S / B2
-    const float d_s12 = 2.0f * A1 * inv;
-    const float SB2 = S * B2;
-    const float d_mu1 = 2.0f * inv * (mu2 * A2 - mu1 * SB2);
-    const float d_mu2 = 2.0f * inv * (mu1 * A2 - mu2 * SB2);
-    g.g_m1 = d_mu1 - 2.0f * m.m1 * d_ss - m.m2 * d_s12;
-    g.g_m2 = d_mu2 - 2.0f * m.m2 * d_ss - m.m1 * d_s12;
-    g.g_e = d_ss;
-    g.g_e12 = d_s12;
+    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
+    const float A2 = fmaf(2.0f, s12, kC2);
+    const float r1 = rcp_approx(B1), r2 = rcp_approx(B2);
+    const float2 lc = __fmul2_rn(make_float2(A1, A2), make_float2(r1, r2));
+    const float l = valid ? lc.x : 0.0f, cs = valid ? lc.y : 0.0f;
+    const float S = l * cs;
+    const float lr2 = l * r2;
+    g.g_e = -cs * lr2;
+    g.g_e12 = lr2 + lr2;
+    const float cr1x2 = cs * (r1 + r1);
+    g.g_m1 = fmaf(cr1x2, fmaf(-mu.x, l, mu.y), g.g_e12 * fmaf(m.m1, cs, -m.m2));
+    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-mu.y, l, mu.x), g.g_e12 * fmaf(m.m2, cs, -m.m1));
     return S;
 }
 

@@ -16,10 +16,10 @@
 //   V  column pass, one thread per column: an 11-row register ring of hb gives
 //      the window statistics, then SSIM and its derivatives in registers; in
 //      gradient mode a second 11-row register ring of those derivatives gives
-//      the column pass of the adjoint (vb);
-//   A  row pass of the adjoint over vb and the chain rule with the input pixel
-//      (re-read from L1 / L2); the gradient row is staged in shared memory and
-//      stored, one column per thread, during the next V.
+//      the column pass of the adjoint (va, vc);
+//   A  row pass of the adjoint over va / vc, the chain rule with the input
+//      pixels of the gradient rows (prefetched into cb by cp.async while V
+//      runs), and the store of the gradient.
 // H of step t+1 and A of step t share one barrier interval.  Streaming down the
 // rows computes every statistic of the strip once (no vertical halo recompute
 // except the 20-row warm-up of a segment).
@@ -47,17 +47,21 @@ constexpr int SWG = GW + 10;           // gradient mode: statistic columns per s
 constexpr int GSHIFT = 2;              // gradient strips start at column GW * s - GSHIFT
 constexpr int IWP = 140;               // float pitch of a staged input row (35 x 16 bytes)
 constexpr int STEP = kTaps;            // rows per step = ring length
-constexpr int RP = NT + 1;             // float4 pitch of a row of hb / vb (one pad slot)
-constexpr int RBUF = STEP * RP + 1;    // hb / vb size in float4 (a guard slot at the end)
+constexpr int RP = NT + 1;             // float4 pitch of a row of hb (one pad slot)
+constexpr int HBUF = STEP * RP + 1;    // hb size in float4
 constexpr int KA = 8;                  // columns per adjoint row-pass work item
 constexpr int NGA = (GW + KA - 1) / KA;
-constexpr int GWP = 124;               // float pitch of a staged gradient row
+constexpr int P2 = 130;                // float2 pitch of the adjoint pair planes
+constexpr int P1 = 132;                // float pitch of the single adjoint plane
+constexpr int CBP = 122;               // float pitch of the chain-rule pixel rows
+constexpr int CBOFF = 2;               // gradient column jj sits at cb column jj + CBOFF
 constexpr int NBUF = 2;                // input row blocks in flight
 
 static_assert(SWG <= NT, "one thread per statistic column");
 static_assert(IWP % 4 == 0 && IWP >= SW + 10 && IWP >= GW + 20, "input pitch");
-static_assert(GWP % 4 == 0 && GWP >= NGA * KA, "gradient staging pitch");
-static_assert((NGA - 1) * KA + KA + 9 <= NT + 1, "adjoint reads stay within a row + guard");
+static_assert((NGA - 1) * KA + KA + 9 < P2 && (NGA - 1) * KA + KA + 12 <= P1,
+              "adjoint reads stay within a row");
+static_assert(CBP % 2 == 0 && CBP >= NGA * KA + CBOFF, "chain-rule pixel pitch");
 static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
               "gradient strips stage from 16-byte aligned columns");
 
@@ -67,21 +71,43 @@ static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
 // or entirely outside the image.  Otherwise a 4-byte path stages them.
 __device__ __forceinline__ int stat_shift(int off) { return (4 - (off & 3)) & 3; }
 
-// Shared memory: xs, ys [NBUF][STEP][IWP] floats, hb [RBUF] float4, then in
-// gradient mode vb [RBUF] float4 and sg [1 or 2][STEP][GWP] floats.
+// Shared memory (byte offsets):
+//   xs, ys  [NBUF][STEP][IWP] float       input rows
+//   hb      [HBUF] float4                  row-blurred statistics (m1, m2, es, e12)
+// gradient mode only:
+//   va      [STEP][P2] float2              adjoint column sums (g_m1, g_e)
+//   vb2     [STEP][P2] float2              (g_e12, g_m2)        [grad2]
+//   vc      [STEP][P1] float               g_e12                [grad1 only]
+//   cbx,cby [STEP][CBP] float              input pixels of this step's gradient rows
 // Work items of the row passes are numbered row-fastest (item = g * STEP + k),
 // so the eight threads of a quarter warp mostly touch eight consecutive rows;
-// with the odd pitches (RP float4 = 129, GWP = 31 float4, IWP = 35 float4) those
-// land in distinct bank groups, and every address inside an item is a base plus
-// a compile-time offset.
+// the odd pitches (in 16-byte units: IWP 35, RP 129, P2 65, P1 33) put those in
+// distinct bank groups, and every address inside an item is a base plus a
+// compile-time offset.
 constexpr size_t kInBytes = size_t(2) * NBUF * STEP * IWP * sizeof(float);
-constexpr size_t kRowBytes = size_t(RBUF) * sizeof(float4);
-constexpr size_t kStageBytes = size_t(STEP) * GWP * sizeof(float);
+constexpr size_t kHbBytes = size_t(HBUF) * sizeof(float4);
+constexpr size_t kPairPlane = size_t(STEP) * P2 * sizeof(float2);
+constexpr size_t kOnePlane = size_t(STEP) * P1 * sizeof(float);
+constexpr size_t kCbBytes = size_t(2) * STEP * CBP * sizeof(float);
+
+__host__ __device__ constexpr size_t smem_bytes_for(bool grad, bool g2)
+{
+    return kInBytes + kHbBytes + (grad ? kPairPlane + (g2 ? kPairPlane : kOnePlane) + kCbBytes : 0);
+}
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
 __device__ __forceinline__ float2 lo(const float4 &v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi(const float4 &v) { return make_float2(v.z, v.w); }
+
+__device__ __forceinline__ void cp_async8(void *smem, const void *gmem, bool in_bounds)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    const int src_bytes = in_bounds ? 8 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(s), "l"(gmem),
+                 "r"(src_bytes)
+                 : "memory");
+}
 
 // sum_a w_a r[(N + 1 + a) % 11] (the oldest entry gets w_0) through the symmetry
 // w_a = w_{10-a}: w_5 r_5 + sum_{a<5} w_a (r_a + r_{10-a}).
@@ -122,9 +148,12 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     float *xs = reinterpret_cast<float *>(smem_raw);
     float *ys = xs + NBUF * STEP * IWP;
     float4 *hb = reinterpret_cast<float4 *>(smem_raw + kInBytes);
-    float4 *vb = hb + RBUF;
-    float *sg1 = reinterpret_cast<float *>(smem_raw + kInBytes + 2 * kRowBytes);
-    float *sg2 = sg1 + STEP * GWP;
+    unsigned char *gbase = smem_raw + kInBytes + kHbBytes;
+    float2 *va = reinterpret_cast<float2 *>(gbase);
+    float2 *vb2 = reinterpret_cast<float2 *>(gbase + kPairPlane);
+    float *vc = reinterpret_cast<float *>(gbase + kPairPlane);
+    float *cbx = reinterpret_cast<float *>(gbase + kPairPlane + (G2 ? kPairPlane : kOnePlane));
+    float *cby = cbx + STEP * CBP;
     __shared__ double red[NT / 32];
 
     const int tid = threadIdx.x;
@@ -202,6 +231,37 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         }
     };
 
+    // ---- the input pixels of the gradient rows of step t: rows R0 + 11 t - 10 + k,
+    //      gradient columns jj at cb column jj + CBOFF (zeros outside the image)
+    auto load_chain = [&](int t) {
+        const int qb = R0 + t * STEP - 10;
+        if (a.vec16) {
+            // pairs of columns from j0 - CBOFF (even): 8-byte copies, each pair
+            // entirely inside or outside the image (W even)
+            constexpr int NPAIR = (NGA * KA + CBOFF) / 2;
+            for (int e = tid; e < STEP * NPAIR; e += NT) {
+                const int k = e / NPAIR, pr = e - k * NPAIR;
+                const int q = qb + k, j = j0 - CBOFF + 2 * pr;
+                const bool inb = (q >= 0) && (q < a.H) && (j >= 0) && (j < a.W);
+                const size_t gi = inb ? size_t(q) * a.W + j : 0;
+                cp_async8(cbx + k * CBP + 2 * pr, xp + gi, inb);
+                cp_async8(cby + k * CBP + 2 * pr, yp + gi, inb);
+            }
+            return;
+        }
+        const int j = j0 + tid;
+        const bool cin = (tid < GW) && (j >= 0) && (j < a.W);
+        for (int k = 0; k < STEP; ++k) {
+            const int q = qb + k;
+            const bool inb = cin && (q >= 0) && (q < a.H);
+            const size_t gi = inb ? size_t(q) * a.W + j : 0;
+            if (tid < GW) {
+                cp_async4(cbx + k * CBP + CBOFF + tid, xp + gi, inb);
+                cp_async4(cby + k * CBP + CBOFF + tid, yp + gi, inb);
+            }
+        }
+    };
+
     // ---- row pass of the statistics: row k of block t, columns [KH g, KH g + KH)
     auto h_item = [&](int t, int item) {
         const int g = item / STEP, k = item - g * STEP;
@@ -248,79 +308,106 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
 
     const float scale = (GRAD && a.dL) ? a.dL[n] * a.inv_count : a.inv_count;
 
-    // ---- row pass of the adjoint for the gradient row of (block t, row k) and the
-    //      chain rule (input pixels re-read through L1 / L2); results to sg1 / sg2.
-    auto a_item = [&](int t, int item) {
+    // ---- row pass of the adjoint for the gradient row of (step a_step, row k), the
+    //      chain rule with the prefetched pixels, and the store of the gradient
+    int a_step = 0;
+    auto a_item = [&](int item) {
         const int g = item / STEP, k = item - g * STEP;
-        const int q = R0 + t * STEP + k - 10;
+        const int q = R0 + (a_step * STEP) + k - 10;
         if (q < q0 || q >= q1) return;
-        const float4 *src = vb + k * RP + g * KA;
-        // the input pixels of the chain rule, fetched first (through L1 / L2)
-        const size_t rowg = size_t(q) * a.W;
-        float xq[KA], yq[KA];
-#pragma unroll
-        for (int o = 0; o < KA; ++o) {
-            const int jj = g * KA + o, j = j0 + jj;
-            const bool in = (jj < GW) && (j >= 0) && (j < a.W);
-            xq[o] = in ? __ldg(xp + rowg + j) : kShift;
-            yq[o] = in ? __ldg(yp + rowg + j) : kShift;
-        }
         float2 accA[KA];             // (B^T g_m1, B^T g_e)
         float2 accB[KA];             // (B^T g_e12, B^T g_m2)   [G2]
         float accC[KA];              // B^T g_e12              [grad1 only]
+        const float2 *pa = va + k * P2 + g * KA;   // 16-byte aligned (g * KA even)
 #pragma unroll
-        for (int m = 0; m < KA + 10; ++m) {
-            const float4 v = src[m];  // past the strip (or into the guard) only for unused outputs
+        for (int m = 0; m < KA + 10; m += 2) {
+            const float4 u = *reinterpret_cast<const float4 *>(pa + m);  // columns m, m+1
 #pragma unroll
-            for (int o = 0; o < KA; ++o) {
-                const int b = m - o;
-                if (b < 0 || b > 10) continue;
-                const float2 w = splat(tap(b));
-                if (b == 0) {
-                    accA[o] = __fmul2_rn(w, lo(v));
-                    if (G2) accB[o] = __fmul2_rn(w, hi(v)); else accC[o] = w.x * v.z;
-                } else {
-                    accA[o] = __ffma2_rn(w, lo(v), accA[o]);
-                    if (G2) accB[o] = __ffma2_rn(w, hi(v), accB[o]); else accC[o] = fmaf(w.x, v.z, accC[o]);
+            for (int h = 0; h < 2; ++h) {
+                const float2 v = h ? hi(u) : lo(u);
+#pragma unroll
+                for (int o = 0; o < KA; ++o) {
+                    const int b = m + h - o;
+                    if (b < 0 || b > 10) continue;
+                    const float2 w = splat(tap(b));
+                    accA[o] = (b == 0) ? __fmul2_rn(w, v) : __ffma2_rn(w, v, accA[o]);
                 }
             }
         }
+        if (G2) {
+            const float2 *pq = vb2 + k * P2 + g * KA;
+#pragma unroll
+            for (int m = 0; m < KA + 10; m += 2) {
+                const float4 u = *reinterpret_cast<const float4 *>(pq + m);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 v = h ? hi(u) : lo(u);
+#pragma unroll
+                    for (int o = 0; o < KA; ++o) {
+                        const int b = m + h - o;
+                        if (b < 0 || b > 10) continue;
+                        const float2 w = splat(tap(b));
+                        accB[o] = (b == 0) ? __fmul2_rn(w, v) : __ffma2_rn(w, v, accB[o]);
+                    }
+                }
+            }
+        } else {
+            const float *pc = vc + k * P1 + g * KA;  // 16-byte aligned
+#pragma unroll
+            for (int m = 0; m < KA + 12; m += 4) {
+                const float4 u = *reinterpret_cast<const float4 *>(pc + m);
+                const float uv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+#pragma unroll
+                    for (int o = 0; o < KA; ++o) {
+                        const int b = m + h - o;
+                        if (b < 0 || b > 10) continue;
+                        accC[o] = (b == 0) ? tap(b) * uv[h] : fmaf(tap(b), uv[h], accC[o]);
+                    }
+                }
+            }
+        }
+        // chain rule with the prefetched pixels (cb columns jj + CBOFF: 8-byte aligned)
+        const float *px = cbx + k * CBP + CBOFF + g * KA;
+        const float *py = cby + k * CBP + CBOFF + g * KA;
         float r1[KA], r2[KA];
 #pragma unroll
-        for (int o = 0; o < KA; ++o) {
-            const float x = xq[o] - kShift, y = yq[o] - kShift;
-            const float e12 = G2 ? accB[o].x : accC[o];
-            r1[o] = scale * fmaf(2.0f * x, accA[o].y, fmaf(y, e12, accA[o].x));
-            if (G2) r2[o] = scale * fmaf(2.0f * y, accA[o].y, fmaf(x, e12, accB[o].y));
+        for (int o = 0; o < KA; o += 2) {
+            const float2 xx = *reinterpret_cast<const float2 *>(px + o);
+            const float2 yy = *reinterpret_cast<const float2 *>(py + o);
+            const float xo[2] = {xx.x - kShift, xx.y - kShift};
+            const float yo[2] = {yy.x - kShift, yy.y - kShift};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int oo = o + h;
+                const float e12 = G2 ? accB[oo].x : accC[oo];
+                r1[oo] = scale * fmaf(2.0f * xo[h], accA[oo].y, fmaf(yo[h], e12, accA[oo].x));
+                if (G2) r2[oo] = scale * fmaf(2.0f * yo[h], accA[oo].y, fmaf(xo[h], e12, accB[oo].y));
+            }
         }
-        float *d1 = sg1 + k * GWP + g * KA;
+        const size_t rowg = plane_off + size_t(q) * a.W;
+        if (a.vec16) {
+            // j0 + KA g is even and W is even: pairs are 8-byte aligned, inside or outside together
 #pragma unroll
-        for (int o = 0; o < KA; o += 4)
-            *reinterpret_cast<float4 *>(d1 + o) = make_float4(r1[o], r1[o + 1], r1[o + 2], r1[o + 3]);
-        if (G2) {
-            float *d2 = sg2 + k * GWP + g * KA;
+            for (int o = 0; o < KA; o += 2) {
+                const int jj = g * KA + o, j = j0 + jj;
+                if (jj < GW && j >= 0 && j < a.W) {
+                    *reinterpret_cast<float2 *>(a.out1 + rowg + j) = make_float2(r1[o], r1[o + 1]);
+                    if (G2) *reinterpret_cast<float2 *>(a.out2 + rowg + j) = make_float2(r2[o], r2[o + 1]);
+                }
+            }
+        } else {
 #pragma unroll
-            for (int o = 0; o < KA; o += 4)
-                *reinterpret_cast<float4 *>(d2 + o) = make_float4(r2[o], r2[o + 1], r2[o + 2], r2[o + 3]);
+            for (int o = 0; o < KA; ++o) {
+                const int jj = g * KA + o, j = j0 + jj;
+                if (jj < GW && j >= 0 && j < a.W) {
+                    a.out1[rowg + j] = r1[o];
+                    if (G2) a.out2[rowg + j] = r2[o];
+                }
+            }
         }
     };
-
-    // ---- store the staged gradient rows of step t (one column per thread)
-    const int jcol = j0 + tid;
-    const bool store_col = GRAD && (tid < GW) && (jcol >= 0) && (jcol < a.W);
-    auto store_rows = [&](int t) {
-        if (!store_col) return;
-        const int qb = R0 + t * STEP - 10;
-#pragma unroll
-        for (int k = 0; k < STEP; ++k) {
-            const int q = qb + k;
-            if (q < q0 || q >= q1) continue;
-            const size_t gi = plane_off + size_t(q) * a.W + jcol;
-            a.out1[gi] = sg1[k * GWP + tid];
-            if (G2) a.out2[gi] = sg2[k * GWP + tid];
-        }
-    };
-
     // ---- column pass state: registers of thread tid (statistic column sc0 + tid)
     float2 hA[STEP], hB[STEP];   // row-blurred (m1, m2), (es, e12)
     float2 gA[STEP];             // (g_m1, g_e)
@@ -340,6 +427,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
 
     // ---- prologue
     load_block(0);
+    if (GRAD) load_chain(0);
     cp_async_commit();
     if (steps > 1) load_block(1);
     cp_async_commit();
@@ -353,36 +441,36 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         const float4 h = hb[k * RP + tid];
         hA[k] = lo(h);
         hB[k] = hi(h);
+        if (k < klo) {
+            // warm-up row: its window is not complete; nothing downstream reads
+            // its results, only the ring entries must be set
+            gA[k] = gB[k] = f2(0.f, 0.f);
+            gC[k] = 0.f;
+            return;
+        }
+        const bool ok = col_ok && (k < khi);
+        const int p = R0 + t * STEP + k + a.off - 10;
         const float2 M = ring_sum2<k>(hA);
         const float2 E = ring_sum2<k>(hB);
         const Moments mo{M.x, M.y, E.x, E.y};
-        const bool ok = col_ok && (k >= klo) && (k < khi);
-        const int p = R0 + t * STEP + k + a.off - 10;
         if (GRAD) {
             MomentGrads gg;
-            const float S = ssim_and_grads(mo, gg);
-            gA[k] = ok ? f2(gg.g_m1, gg.g_e) : f2(0.f, 0.f);
-            if (G2) gB[k] = ok ? f2(gg.g_e12, gg.g_m2) : f2(0.f, 0.f);
-            else gC[k] = ok ? gg.g_e12 : 0.f;
-            if (want_mean && ok && col_own && k >= kown) {
-                ssum += S;
-                if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
+            const float S = ssim_and_grads<G2>(mo, ok, gg);
+            gA[k] = f2(gg.g_m1, gg.g_e);
+            if (G2) gB[k] = f2(gg.g_e12, gg.g_m2);
+            else gC[k] = gg.g_e12;
+            if (want_mean) {
+                const bool own = ok && col_own && (k >= kown);
+                ssum += own ? S : 0.0f;
+                if (a.map && own) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
             }
-            const float2 vA = ring_sum2<k>(gA);
-            float4 v;
-            if (G2) {
-                const float2 vB = ring_sum2<k>(gB);
-                v = make_float4(vA.x, vA.y, vB.x, vB.y);
-            } else {
-                v = make_float4(vA.x, vA.y, ring_sum1<k>(gC), 0.f);
-            }
-            vb[k * RP + tid] = v;
+            va[k * P2 + tid] = ring_sum2<k>(gA);
+            if (G2) vb2[k * P2 + tid] = ring_sum2<k>(gB);
+            else vc[k * P1 + tid] = ring_sum1<k>(gC);
         } else {
             const float S = ssim_value(mo);
-            if (ok) {
-                ssum += S;
-                if (a.map) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
-            }
+            ssum += ok ? S : 0.0f;
+            if (a.map && ok) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
         }
     };
 
@@ -393,8 +481,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         klo = max(max(0, R0 + 10 - rb), -pb);
         khi = min(min(STEP, Rend - rb), a.Ho - pb);
         kown = (GRAD && seg != 0) ? q0 + 10 - rb : 0;  // q = r - 10 >= q0
-        // ---- V: column passes of step t, and the stores of step t-1's gradient rows
-        if (GRAD && t > 0) store_rows(t - 1);
+        // ---- V: column passes of step t
         v_row(std::integral_constant<int, 0>{}, t);
         v_row(std::integral_constant<int, 1>{}, t);
         v_row(std::integral_constant<int, 2>{}, t);
@@ -406,23 +493,28 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         v_row(std::integral_constant<int, 8>{}, t);
         v_row(std::integral_constant<int, 9>{}, t);
         v_row(std::integral_constant<int, 10>{}, t);
-        cp_async_wait<0>();  // block t+1 has landed
+        cp_async_wait<0>();  // block t+1 and the chain-rule pixels of step t have landed
         __syncthreads();
-        // ---- H of step t+1 and A of step t
-        const int nh = (t + 1 < steps) ? STEP * NGH : 0;
+        // ---- H of step t+1 and A of step t.  The row-pass items are counted in
+        //      whole warps (NHP) so that no warp runs both kinds in one round.
+        constexpr int NHP = (STEP * NGH + 31) / 32 * 32;
+        const int nh = (t + 1 < steps) ? NHP : 0;
         const int na = GRAD ? STEP * NGA : 0;
+        a_step = t;
         for (int i = tid; i < nh + na; i += NT) {
-            if (i < nh)
-                h_item(t + 1, i);
-            else
-                a_item(t, i - nh);
+            if (i < nh) {
+                if (i < STEP * NGH) h_item(t + 1, i);
+            } else {
+                a_item(i - nh);
+            }
         }
         __syncthreads();
-        if (t + 2 < steps) load_block(t + 2);  // into block t's buffer, read by H(t) long ago
+        // block t's buffer (read by H(t) long ago) and cb (just read by A(t)) are free
+        if (t + 2 < steps) load_block(t + 2);
+        if (GRAD && t + 1 < steps) load_chain(t + 1);
         cp_async_commit();
     }
     cp_async_wait<0>();
-    if (GRAD) store_rows(steps - 1);  // the last staged rows (the final barrier above orders them)
 
     if (want_mean) {
         const double tot = block_sum<NT>(ssum, red);
@@ -467,10 +559,7 @@ __global__ void __launch_bounds__(256) scale_fields_scalar(const float *f1, cons
     }
 }
 
-size_t smem_bytes(bool grad, bool g2)
-{
-    return kInBytes + (grad ? 2 * kRowBytes + (g2 ? 2 : 1) * kStageBytes : kRowBytes);
-}
+size_t smem_bytes(bool grad, bool g2) { return smem_bytes_for(grad, g2); }
 
 template <bool GRAD, bool G2>
 cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)

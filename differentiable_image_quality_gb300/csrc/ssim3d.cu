@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
             float S;
             if (GRAD) {
                 MomentGrads gg;
-                S = ssim_and_grads(mo, gg);
+                S = ssim_and_grads<true>(mo, true, gg);
                 const size_t oi = ((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px;
                 reinterpret_cast<float4 *>(a.gfield)[oi] = make_float4(gg.g_m1, gg.g_e, gg.g_e12, gg.g_m2);
             } else {
