@@ -56,7 +56,7 @@ KERNEL3D_NAME = "ssim3d_stats_kernel<true> + ssim3d_adjoint_kernel<false>"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -82,7 +82,7 @@ def measured_peaks():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms meanwhile."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms meanwhile."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -100,7 +100,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
