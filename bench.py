@@ -244,6 +244,23 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, steps: int, max_ms: float) -> float:
+    """Units processed by all ranks per second, over the slowest rank's time."""
+    return world * units_per_rank * steps / (max_ms / 1e3)
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "differentiable_image_quality_gb300", "csrc")
@@ -342,12 +359,8 @@ def run_ours(args):
     clk = clocks.summary()
 
     step_ms = [a + b for a, b in zip(ta, tb)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * mp * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = whole_job_rate(mp, world, args.steps, total_ms)
     fwd_ms = statistics.mean(ta)
     bwd_ms = statistics.mean(tb)
 
@@ -370,12 +383,8 @@ def run_ours(args):
         hm.copy_(mean, non_blocking=True)
 
     te, _ = timed(e2e_step, None, args.steps, max(3, args.warmup))
-    e2e_ms = sum(te)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * mp * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(sum(te), world, dev)
+    e2e_value = whole_job_rate(mp, world, args.steps, e2e_ms)
 
     extras = {}
     if not args.no_extras:
