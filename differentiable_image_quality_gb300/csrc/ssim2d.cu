@@ -53,7 +53,7 @@ constexpr int KA = 8;                  // columns per adjoint row-pass work item
 constexpr int NGA = (GW + KA - 1) / KA;
 constexpr int P2 = 130;                // float2 pitch of the adjoint pair planes
 constexpr int P1 = 132;                // float pitch of the single adjoint plane
-constexpr int CBP = 122;               // float pitch of the chain-rule pixel rows
+constexpr int CBP = 124;               // float pitch of the chain-rule pixel rows (16-byte rows)
 constexpr int CBOFF = 2;               // gradient column jj sits at cb column jj + CBOFF
 constexpr int NBUF = 2;                // input row blocks in flight
 
@@ -61,7 +61,9 @@ static_assert(SWG <= NT, "one thread per statistic column");
 static_assert(IWP % 4 == 0 && IWP >= SW + 10 && IWP >= GW + 20, "input pitch");
 static_assert((NGA - 1) * KA + KA + 9 < P2 && (NGA - 1) * KA + KA + 12 <= P1,
               "adjoint reads stay within a row");
-static_assert(CBP % 2 == 0 && CBP >= NGA * KA + CBOFF, "chain-rule pixel pitch");
+static_assert(CBP % 4 == 0 && CBP >= NGA * KA + CBOFF, "chain-rule pixel pitch");
+static_assert((GW - GSHIFT - CBOFF) % 4 == 0 && (GSHIFT + CBOFF) % 4 == 0,
+              "chain-rule rows start on a 16-byte boundary (column j0 - CBOFF)");
 static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
               "gradient strips stage from 16-byte aligned columns");
 
@@ -99,15 +101,6 @@ __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
 __device__ __forceinline__ float2 lo(const float4 &v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi(const float4 &v) { return make_float2(v.z, v.w); }
-
-__device__ __forceinline__ void cp_async8(void *smem, const void *gmem, bool in_bounds)
-{
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    const int src_bytes = in_bounds ? 8 : 0;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(s), "l"(gmem),
-                 "r"(src_bytes)
-                 : "memory");
-}
 
 // sum_a w_a r[(N + 1 + a) % 11] (the oldest entry gets w_0) through the symmetry
 // w_a = w_{10-a}: w_5 r_5 + sum_{a<5} w_a (r_a + r_{10-a}).
@@ -236,16 +229,16 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     auto load_chain = [&](int t) {
         const int qb = R0 + t * STEP - 10;
         if (a.vec16) {
-            // pairs of columns from j0 - CBOFF (even): 8-byte copies, each pair
-            // entirely inside or outside the image (W even)
-            constexpr int NPAIR = (NGA * KA + CBOFF) / 2;
-            for (int e = tid; e < STEP * NPAIR; e += NT) {
-                const int k = e / NPAIR, pr = e - k * NPAIR;
-                const int q = qb + k, j = j0 - CBOFF + 2 * pr;
+            // 16-byte chunks from column j0 - CBOFF (a multiple of 4): each chunk
+            // entirely inside or outside the image (W % 4 == 0)
+            constexpr int NCH = (NGA * KA + CBOFF + 3) / 4;
+            for (int e = tid; e < STEP * NCH; e += NT) {
+                const int k = e / NCH, ch = e - k * NCH;
+                const int q = qb + k, j = j0 - CBOFF + 4 * ch;
                 const bool inb = (q >= 0) && (q < a.H) && (j >= 0) && (j < a.W);
                 const size_t gi = inb ? size_t(q) * a.W + j : 0;
-                cp_async8(cbx + k * CBP + 2 * pr, xp + gi, inb);
-                cp_async8(cby + k * CBP + 2 * pr, yp + gi, inb);
+                cp_async16(cbx + k * CBP + 4 * ch, xp + gi, inb);
+                cp_async16(cby + k * CBP + 4 * ch, yp + gi, inb);
             }
             return;
         }
