@@ -192,7 +192,7 @@ struct Plan3d {
     long long blocks = 0;
 };
 
-// Tiles of 16 x 32 columns over (rows, cols), z segments over zlen, with the
+// Tiles of 16 x 16 columns over (rows, cols), z segments over zlen, with the
 // same per-SM cost model as in 2D (a 10-slice warm-up per segment).
 Plan3d plan3d(long long planes, int zlen, int rows, int cols, int sm_count, int occ)
 {
@@ -434,6 +434,10 @@ static void fill3d(Ssim3dArgs &a, const float *x, const float *y, int N, int C, 
     a.Do = out_extent(D, padding); a.Ho = out_extent(H, padding); a.Wo = out_extent(W, padding);
     a.off = padding == GBSSIM_VALID ? 0 : kRadius;
     a.C = C;
+    // 16-byte staging of the statistics kernel: tile origins (multiples of 16
+    // minus off) on 16-byte boundaries, 16-byte row pitch, aligned volumes
+    a.vec16 = (a.off % 4 == 0) && (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     const Layout3d l = layout3d(N, C, D, H, W, padding);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.counter = reinterpret_cast<unsigned *>(ws);

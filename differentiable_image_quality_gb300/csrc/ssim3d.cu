@@ -3,7 +3,7 @@
 //
 // Following that page's plan -- keep the 2D convolution on XY slices, and do
 // the Z convolution and SSIM through a ring buffer, one depth row per thread --
-// a CTA owns an XY tile of 16 x 32 columns and walks along Z one slice per step:
+// a CTA owns an XY tile of 16 x 16 columns and walks along Z one slice per step:
 //   XY  the slice's row pass and column pass in shared memory (cp.async staging
 //       of the slice tile plus its 10-pixel halo, three buffers);
 //   Z   each thread keeps an 11-slice register ring of its column's XY-blurred
@@ -16,56 +16,91 @@
 //            the blur with the window mirrored, which for a symmetric window is
 //            the same correlation with the "full" extent), then the chain rule
 //            grad1 = B^T g_mu1 + 2 x B^T g_e + y B^T g_e12 (grad2 likewise).
+// All window sums run on float pairs (fma.rn.f32x2): (mu1, mu2), (es, e12) for
+// the statistics, (g_mu1, g_e), (g_e12, g_mu2) for the adjoint.  Work items of
+// the row passes are numbered row-fastest over odd shared-memory pitches, so
+// the threads of a quarter warp hit distinct bank groups.
 #include "common.cuh"
 #include "ssim3d.cuh"
 
 namespace gbssim {
 namespace {
 
-constexpr int NT = kThreads3d;  // 512
-constexpr int TY = kTile3dY;    // 16 rows of columns per tile
-constexpr int TX = kTile3dX;    // 32 columns per row
-constexpr int IY = TY + 10, IX = TX + 10;
-constexpr int IXP = IX + 2;     // float pitch of the staged input rows (float4 aligned)
-constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;  // row-pass items per slice
-constexpr int KY = 4, NYG = TY / KY, NYI = NYG * TX;  // column-pass items per slice
+constexpr int NT = kThreads3d;   // 256
+constexpr int TY = kTile3dY;     // 16 rows of columns per tile
+constexpr int TX = kTile3dX;     // 16 columns per row
+constexpr int IY = TY + 10, IX = TX + 10;   // 26 x 26 staged slice tile
+constexpr int IXP = 28;          // float pitch of a staged input row (7 x 16 bytes)
+constexpr int GXP = IX + 1;      // float4 pitch of a staged derivative row (27)
+constexpr int HXP = TX + 1;      // float4 pitch of a row-pass output row (17)
+constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;   // row-pass items per slice (104)
+constexpr int KY = 2, NYG = TY / KY, NYI = NYG * TX;   // column-pass items per slice (128)
 constexpr int NBUF = 3;
 
 static_assert(NT == TY * TX, "one thread per column of the tile");
+static_assert(NYI % 32 == 0, "column-pass items fill whole warps");
+static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
 
 constexpr size_t kStatsInBytes = size_t(2) * NBUF * IY * IXP * sizeof(float);
-constexpr size_t kAdjInBytes = size_t(NBUF) * IY * IX * sizeof(float4);
-constexpr size_t kXBytes = size_t(2) * IY * TX * sizeof(float4);
+constexpr size_t kAdjInBytes = size_t(NBUF) * IY * GXP * sizeof(float4);
+constexpr size_t kXBytes = size_t(2) * IY * HXP * sizeof(float4);
 constexpr size_t kYBytes = size_t(TY) * TX * sizeof(float4);
 
-__device__ __forceinline__ int swz(int c) { return (c & ~7) | ((c + (c >> 3)) & 7); }
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
+__device__ __forceinline__ float2 lo(const float4 &v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi(const float4 &v) { return make_float2(v.z, v.w); }
 
-__device__ __forceinline__ float4 wsum_ring(const float4 (&ring)[kTaps], int newest)
+// sum_a w_a r[(N + 1 + a) % 11] (the oldest entry gets w_0), symmetric taps.
+template <int N>
+__device__ __forceinline__ float2 ring_sum2(const float2 (&r)[kTaps])
 {
-    // sum_a w_a ring[(newest + 1 + a) % 11]: the oldest slice gets w_0
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc = __fmul2_rn(splat(tap(5)), r[(N + 6) % kTaps]);
 #pragma unroll
-    for (int a = 0; a < kTaps; ++a) {
-        const float4 h = ring[(newest + 1 + a) % kTaps];
-        const float w = tap(a);
-        s.x = fmaf(w, h.x, s.x);
-        s.y = fmaf(w, h.y, s.y);
-        s.z = fmaf(w, h.z, s.z);
-        s.w = fmaf(w, h.w, s.w);
-    }
-    return s;
+    for (int a = 0; a < 5; ++a)
+        acc = __ffma2_rn(splat(tap(a)), __fadd2_rn(r[(N + 1 + a) % kTaps], r[(N + 11 - a) % kTaps]),
+                         acc);
+    return acc;
 }
+
+// 11-tap pass over float4 values loaded from smem at src[stride * m],
+// m = 0 .. K + 9, giving K outputs (two float pairs each).
+template <int K>
+__device__ __forceinline__ void taps4(const float4 *src, int stride, float2 (&oa)[K], float2 (&ob)[K])
+{
+#pragma unroll
+    for (int m = 0; m < K + 10; ++m) {
+        const float4 v = src[m * stride];
+#pragma unroll
+        for (int o = 0; o < K; ++o) {
+            const int t = m - o;
+            if (t < 0 || t > 10) continue;
+            const float2 w = splat(tap(t));
+            oa[o] = (t == 0) ? __fmul2_rn(w, lo(v)) : __ffma2_rn(w, lo(v), oa[o]);
+            ob[o] = (t == 0) ? __fmul2_rn(w, hi(v)) : __ffma2_rn(w, hi(v), ob[o]);
+        }
+    }
+}
+
+// Z-step dispatch: the ring slot is a compile-time constant in each case.
+#define GBSSIM_RING_SWITCH(s, CALL)                                           \
+    switch ((s) % kTaps) {                                                    \
+    case 0: CALL(0); break;  case 1: CALL(1); break;  case 2: CALL(2); break; \
+    case 3: CALL(3); break;  case 4: CALL(4); break;  case 5: CALL(5); break; \
+    case 6: CALL(6); break;  case 7: CALL(7); break;  case 8: CALL(8); break; \
+    case 9: CALL(9); break;  default: CALL(10); break;                        \
+    }
 
 // ------------------------------------------------------------------ kernel A
 
 template <bool GRAD>
-__global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
+__global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *xs = reinterpret_cast<float *>(smem_raw);
     float *ys = xs + NBUF * IY * IXP;
     float4 *hx = reinterpret_cast<float4 *>(smem_raw + kStatsInBytes);
-    float4 *hy = hx + 2 * IY * TX;
+    float4 *hy = hx + 2 * IY * HXP;
     __shared__ double red[NT / 32];
 
     const int tid = threadIdx.x;
@@ -88,6 +123,21 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
         const int buf = s % NBUF;
         const int Z = iz0 + s;
         const bool zin = (Z >= 0) && (Z < a.D);
+        if (a.vec16) {
+            // the tile origin ix0 is a multiple of 4 and W % 4 == 0: 16-byte chunks,
+            // each entirely inside or outside the volume
+            constexpr int NCH = IXP / 4;
+            for (int e = tid; e < IY * NCH; e += NT) {
+                const int r = e / NCH, ch = e - r * NCH;
+                const int Y = iy0 + r, X = ix0 + 4 * ch;
+                const bool inb = zin && (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
+                const size_t gi = inb ? (size_t(Z) * a.H + Y) * a.W + X : 0;
+                const int si = (buf * IY + r) * IXP + 4 * ch;
+                cp_async16(xs + si, xp + gi, inb);
+                cp_async16(ys + si, yp + gi, inb);
+            }
+            return;
+        }
         for (int e = tid; e < IY * IX; e += NT) {
             const int r = e / IX, c = e - r * IX;
             const int Y = iy0 + r, X = ix0 + c;
@@ -99,9 +149,9 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
         }
     };
 
-    // row pass of slice s: row r of the staged tile, columns [KX g, KX g + KX)
+    // row pass of slice s: staged row r, columns [KX g, KX g + KX)
     auto x_item = [&](int s, int item) {
-        const int r = item / NXG, g = item - r * NXG;
+        const int g = item / IY, r = item - g * IY;
         const int base = ((s % NBUF) * IY + r) * IXP + g * KX;
         float xv[KX + 10], yv[KX + 10];
 #pragma unroll
@@ -117,89 +167,69 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
             xv[KX + 8] = u.x; xv[KX + 9] = u.y;
             yv[KX + 8] = v.x; yv[KX + 9] = v.y;
         }
-        float acc[KX][4];
+        float2 accA[KX], accB[KX];
 #pragma unroll
         for (int m = 0; m < KX + 10; ++m) {
-            const float xx = xv[m] - kShift, yy = yv[m] - kShift;
-            const float pe = fmaf(xx, xx, yy * yy);
-            const float pc = xx * yy;
+            const float2 p = f2(xv[m] - kShift, yv[m] - kShift);
+            const float2 sq = __fmul2_rn(p, p);
+            const float2 q = f2(sq.x + sq.y, p.x * p.y);
 #pragma unroll
             for (int o = 0; o < KX; ++o) {
                 const int t = m - o;
                 if (t < 0 || t > 10) continue;
-                const float w = tap(t);
-                if (t == 0) {
-                    acc[o][0] = w * xx; acc[o][1] = w * yy; acc[o][2] = w * pe; acc[o][3] = w * pc;
-                } else {
-                    acc[o][0] = fmaf(w, xx, acc[o][0]);
-                    acc[o][1] = fmaf(w, yy, acc[o][1]);
-                    acc[o][2] = fmaf(w, pe, acc[o][2]);
-                    acc[o][3] = fmaf(w, pc, acc[o][3]);
-                }
+                const float2 w = splat(tap(t));
+                accA[o] = (t == 0) ? __fmul2_rn(w, p) : __ffma2_rn(w, p, accA[o]);
+                accB[o] = (t == 0) ? __fmul2_rn(w, q) : __ffma2_rn(w, q, accB[o]);
             }
         }
-        float4 *dst = hx + (s & 1) * IY * TX + r * TX;
+        float4 *dst = hx + ((s & 1) * IY + r) * HXP + g * KX;
 #pragma unroll
         for (int o = 0; o < KX; ++o)
-            dst[swz(g * KX + o)] = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+            dst[o] = make_float4(accA[o].x, accA[o].y, accB[o].x, accB[o].y);
     };
 
     // column pass of slice s: column tx, rows [KY g, KY g + KY)
     auto y_item = [&](int s, int item) {
         const int g = item / TX, tx = item - g * TX;
-        const float4 *src = hx + (s & 1) * IY * TX;
-        float4 acc[KY];
+        float2 oa[KY], ob[KY];
+        taps4<KY>(hx + ((s & 1) * IY + g * KY) * HXP + tx, HXP, oa, ob);
 #pragma unroll
-        for (int m = 0; m < KY + 10; ++m) {
-            const float4 v = src[(g * KY + m) * TX + swz(tx)];
-#pragma unroll
-            for (int o = 0; o < KY; ++o) {
-                const int t = m - o;
-                if (t < 0 || t > 10) continue;
-                const float w = tap(t);
-                if (t == 0) {
-                    acc[o] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
-                } else {
-                    acc[o].x = fmaf(w, v.x, acc[o].x);
-                    acc[o].y = fmaf(w, v.y, acc[o].y);
-                    acc[o].z = fmaf(w, v.z, acc[o].z);
-                    acc[o].w = fmaf(w, v.w, acc[o].w);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 0; o < KY; ++o) hy[(g * KY + o) * TX + tx] = acc[o];
+        for (int o = 0; o < KY; ++o)
+            hy[(g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
     };
 
     const int ty = tid / TX, tx = tid - ty * TX;
     const int py = y0 + ty, px = x0 + tx;
     const bool col_ok = (py < a.Ho) && (px < a.Wo);
-    float4 ring[kTaps];
+    float2 rA[kTaps], rB[kTaps];
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) ring[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kTaps; ++k) rA[k] = rB[k] = f2(0.f, 0.f);
     float ssum = 0.0f;
 
     // Z step: push this column's XY-blurred value of slice s, finish slice s - 10.
     auto z_step = [&](auto K_, int s) {
         constexpr int K = decltype(K_)::value;
-        ring[K] = hy[ty * TX + tx];
+        const float4 h = hy[ty * TX + tx];
+        rA[K] = lo(h);
+        rB[K] = hi(h);
         const int p = z0 + s - 10;
         if (s >= 10 && p < z1 && col_ok) {
-            const float4 h = wsum_ring(ring, K);
-            const Moments mo{h.x, h.y, h.z, h.w};
+            const float2 M = ring_sum2<K>(rA), E = ring_sum2<K>(rB);
+            const Moments mo{M.x, M.y, E.x, E.y};
             float S;
+            const size_t oi = ((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px;
             if (GRAD) {
                 MomentGrads gg;
                 S = ssim_and_grads<true>(mo, true, gg);
-                const size_t oi = ((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px;
                 reinterpret_cast<float4 *>(a.gfield)[oi] = make_float4(gg.g_m1, gg.g_e, gg.g_e12, gg.g_m2);
             } else {
                 S = ssim_value(mo);
             }
             ssum += S;
-            if (a.map) a.map[((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px] = S;
+            if (a.map) a.map[oi] = S;
         }
     };
+#define GBSSIM_ZA(K) z_step(std::integral_constant<int, K>{}, s)
 
     load_slice(0);
     cp_async_commit();
@@ -223,22 +253,11 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
         __syncthreads();
         if (s + 3 < nz) load_slice(s + 3);  // into the buffer x_item(s) released
         cp_async_commit();
-        switch (s % kTaps) {
-        case 0: z_step(std::integral_constant<int, 0>{}, s); break;
-        case 1: z_step(std::integral_constant<int, 1>{}, s); break;
-        case 2: z_step(std::integral_constant<int, 2>{}, s); break;
-        case 3: z_step(std::integral_constant<int, 3>{}, s); break;
-        case 4: z_step(std::integral_constant<int, 4>{}, s); break;
-        case 5: z_step(std::integral_constant<int, 5>{}, s); break;
-        case 6: z_step(std::integral_constant<int, 6>{}, s); break;
-        case 7: z_step(std::integral_constant<int, 7>{}, s); break;
-        case 8: z_step(std::integral_constant<int, 8>{}, s); break;
-        case 9: z_step(std::integral_constant<int, 9>{}, s); break;
-        default: z_step(std::integral_constant<int, 10>{}, s); break;
-        }
+        GBSSIM_RING_SWITCH(s, GBSSIM_ZA)
         cp_async_wait<1>();  // slice s + 2 has landed
         __syncthreads();
     }
+#undef GBSSIM_ZA
     cp_async_wait<0>();
 
     if (a.partials) {
@@ -251,12 +270,12 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_stats_kernel(const Ssim3dArgs a)
 // ------------------------------------------------------------------ kernel B
 
 template <bool G2>
-__global__ void __launch_bounds__(NT, 1) ssim3d_adjoint_kernel(const Ssim3dArgs a)
+__global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][IY][IX]
-    float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes);     // [2][IY][TX]
-    float4 *uy = ux + 2 * IY * TX;                                        // [TY][TX]
+    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][IY][GXP]
+    float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes);     // [2][IY][HXP]
+    float4 *uy = ux + 2 * IY * HXP;                                       // [TY][TX]
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -287,83 +306,65 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_adjoint_kernel(const Ssim3dArgs 
             const int Y = gy0 + r, X = gx0 + c;
             const bool inb = zin && (Y >= 0) && (Y < a.Ho) && (X >= 0) && (X < a.Wo);
             const size_t gi = inb ? (size_t(P) * a.Ho + Y) * a.Wo + X : 0;
-            cp_async16(gs + (buf * IY + r) * IX + c, gf + gi, inb);
+            cp_async16(gs + (buf * IY + r) * GXP + c, gf + gi, inb);
         }
     };
 
     // adjoint row pass: gradient columns [KX g, KX g + KX) of staged row r
     auto x_item = [&](int s, int item) {
-        const int r = item / NXG, g = item - r * NXG;
-        const float4 *src = gs + ((s % NBUF) * IY + r) * IX + g * KX;
-        float4 acc[KX];
+        const int g = item / IY, r = item - g * IY;
+        float2 oa[KX], ob[KX];
+        taps4<KX>(gs + ((s % NBUF) * IY + r) * GXP + g * KX, 1, oa, ob);
+        float4 *dst = ux + ((s & 1) * IY + r) * HXP + g * KX;
 #pragma unroll
-        for (int m = 0; m < KX + 10; ++m) {
-            const float4 v = src[m];
-#pragma unroll
-            for (int o = 0; o < KX; ++o) {
-                const int t = m - o;
-                if (t < 0 || t > 10) continue;
-                const float w = tap(t);
-                if (t == 0) {
-                    acc[o] = make_float4(w * v.x, w * v.y, w * v.z, G2 ? w * v.w : 0.f);
-                } else {
-                    acc[o].x = fmaf(w, v.x, acc[o].x);
-                    acc[o].y = fmaf(w, v.y, acc[o].y);
-                    acc[o].z = fmaf(w, v.z, acc[o].z);
-                    if (G2) acc[o].w = fmaf(w, v.w, acc[o].w);
-                }
-            }
-        }
-        float4 *dst = ux + (s & 1) * IY * TX + r * TX;
-#pragma unroll
-        for (int o = 0; o < KX; ++o) dst[swz(g * KX + o)] = acc[o];
+        for (int o = 0; o < KX; ++o) dst[o] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
     };
 
     auto y_item = [&](int s, int item) {
         const int g = item / TX, tx = item - g * TX;
-        const float4 *src = ux + (s & 1) * IY * TX;
-        float4 acc[KY];
+        float2 oa[KY], ob[KY];
+        taps4<KY>(ux + ((s & 1) * IY + g * KY) * HXP + tx, HXP, oa, ob);
 #pragma unroll
-        for (int m = 0; m < KY + 10; ++m) {
-            const float4 v = src[(g * KY + m) * TX + swz(tx)];
-#pragma unroll
-            for (int o = 0; o < KY; ++o) {
-                const int t = m - o;
-                if (t < 0 || t > 10) continue;
-                const float w = tap(t);
-                if (t == 0) {
-                    acc[o] = make_float4(w * v.x, w * v.y, w * v.z, G2 ? w * v.w : 0.f);
-                } else {
-                    acc[o].x = fmaf(w, v.x, acc[o].x);
-                    acc[o].y = fmaf(w, v.y, acc[o].y);
-                    acc[o].z = fmaf(w, v.z, acc[o].z);
-                    if (G2) acc[o].w = fmaf(w, v.w, acc[o].w);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 0; o < KY; ++o) uy[(g * KY + o) * TX + tx] = acc[o];
+        for (int o = 0; o < KY; ++o)
+            uy[(g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
     };
 
     const int ty = tid / TX, tx = tid - ty * TX;
     const int qy = y0 + ty, qx = x0 + tx;
     const bool col_ok = (qy < a.H) && (qx < a.W);
-    float4 ring[kTaps];
+    float2 rA[kTaps], rB[kTaps];
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) ring[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kTaps; ++k) rA[k] = rB[k] = f2(0.f, 0.f);
+
+    // the input pixels of the chain rule, fetched one Z step ahead
+    float xn = 0.f, yn = 0.f;
+    auto fetch = [&](int s) {  // pixels of gradient slice q0 + s - 10
+        const int q = q0 + s - 10;
+        if (col_ok && q >= q0 && q < q1) {
+            const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
+            xn = __ldg(a.x + gi);
+            yn = __ldg(a.y + gi);
+        }
+    };
 
     auto z_step = [&](auto K_, int s) {
         constexpr int K = decltype(K_)::value;
-        ring[K] = uy[ty * TX + tx];
+        const float4 h = uy[ty * TX + tx];
+        rA[K] = lo(h);
+        rB[K] = hi(h);
+        const float xc = xn, yc = yn;  // fetched during the previous step
+        fetch(s + 1);
         const int q = q0 + s - 10;
         if (s >= 10 && q < q1 && col_ok) {
             const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
-            const float x = __ldg(a.x + gi) - kShift, y = __ldg(a.y + gi) - kShift;
-            const float4 v = wsum_ring(ring, K);  // (B^T g_m1, B^T g_e, B^T g_e12, B^T g_m2)
-            a.out1[gi] = scale * fmaf(2.0f * x, v.y, fmaf(y, v.z, v.x));
-            if (G2) a.out2[gi] = scale * fmaf(2.0f * y, v.y, fmaf(x, v.z, v.w));
+            const float x = xc - kShift, y = yc - kShift;
+            const float2 vA = ring_sum2<K>(rA);  // (B^T g_m1, B^T g_e)
+            const float2 vB = ring_sum2<K>(rB);  // (B^T g_e12, B^T g_m2)
+            a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
+            if (G2) a.out2[gi] = scale * fmaf(2.0f * y, vA.y, fmaf(x, vB.x, vB.y));
         }
     };
+#define GBSSIM_ZB(K) z_step(std::integral_constant<int, K>{}, s)
 
     load_slice(0);
     cp_async_commit();
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_adjoint_kernel(const Ssim3dArgs 
     cp_async_commit();
     if (nz > 2) load_slice(2);
     cp_async_commit();
+    fetch(0);
     cp_async_wait<1>();
     __syncthreads();
     for (int i = tid; i < NXI; i += NT) x_item(0, i);
@@ -387,22 +389,11 @@ __global__ void __launch_bounds__(NT, 1) ssim3d_adjoint_kernel(const Ssim3dArgs 
         __syncthreads();
         if (s + 3 < nz) load_slice(s + 3);
         cp_async_commit();
-        switch (s % kTaps) {
-        case 0: z_step(std::integral_constant<int, 0>{}, s); break;
-        case 1: z_step(std::integral_constant<int, 1>{}, s); break;
-        case 2: z_step(std::integral_constant<int, 2>{}, s); break;
-        case 3: z_step(std::integral_constant<int, 3>{}, s); break;
-        case 4: z_step(std::integral_constant<int, 4>{}, s); break;
-        case 5: z_step(std::integral_constant<int, 5>{}, s); break;
-        case 6: z_step(std::integral_constant<int, 6>{}, s); break;
-        case 7: z_step(std::integral_constant<int, 7>{}, s); break;
-        case 8: z_step(std::integral_constant<int, 8>{}, s); break;
-        case 9: z_step(std::integral_constant<int, 9>{}, s); break;
-        default: z_step(std::integral_constant<int, 10>{}, s); break;
-        }
+        GBSSIM_RING_SWITCH(s, GBSSIM_ZB)
         cp_async_wait<1>();
         __syncthreads();
     }
+#undef GBSSIM_ZB
     cp_async_wait<0>();
 }
 

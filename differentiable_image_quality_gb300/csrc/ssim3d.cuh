@@ -6,9 +6,9 @@
 
 namespace gbssim {
 
-constexpr int kThreads3d = 512;
+constexpr int kThreads3d = 256;
 constexpr int kTile3dY = 16;  // tile rows (one thread per column of the tile)
-constexpr int kTile3dX = 32;
+constexpr int kTile3dX = 16;
 
 // Arguments of both 3D kernels.  Grid: one block per (plane, z segment, tile
 // row, tile column), flattened with the tile column fastest.  The statistics
@@ -19,6 +19,7 @@ struct Ssim3dArgs {
     int D, H, W;
     int Do, Ho, Wo;
     int off;                   // 0 valid, 5 same
+    int vec16;                 // statistics staging in 16-byte chunks (see fill3d)
     int C;
     int tiles_x, tiles_y, zsegs, zseg_len;
     float *gfield;             // [planes, Do, Ho, Wo] float4 derivatives (workspace)
