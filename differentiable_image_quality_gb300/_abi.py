@@ -23,6 +23,7 @@ _vp, _sz, _i, _fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_voi
 SIGNATURES = {
     "gbssim_abi_version": (_i, []),
     "gbssim_strerror": (ctypes.c_char_p, [_i]),
+    "gbssim_device_status": (_i, [ctypes.POINTER(ctypes.c_uint)]),
     "gbssim_window": (None, [ctypes.POINTER(ctypes.c_float)]),
     "gbssim_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "gbssim_saved_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -38,8 +39,9 @@ SIGNATURES = {
     "ssim3d_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp, _sz,
                         _vp]),
 }
-# exported beyond the header: the planner's tuning hook
-EXTRA = {"gbssim_tune_seg_rows": (None, [_i])}
+# exported beyond the header: tuning hooks of the planner and of the input
+# staging (the latter also drives the tests of the bounded-wait failure path)
+EXTRA = {"gbssim_tune_seg_rows": (None, [_i]), "gbssim_tune_staging": (None, [_i])}
 
 
 class GbssimError(RuntimeError):

@@ -276,6 +276,18 @@ void gbssim_tune_seg_rows(int rows)
     g_seg_rows_override = rows > 0 ? (rows < kMinSegRows ? kMinSegRows : rows) : 0;
 }
 
+// Tuning and test hook of the 2D input staging: 0 tensor copies where the
+// images allow them (the default), 1 cp.async copies only, 2 tensor copies whose
+// waits are made to run out (exercises the bounded-wait failure path).
+void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
+
+int gbssim_device_status(unsigned *flags_out)
+{
+    if (!flags_out) return GBSSIM_EINVAL;
+    *flags_out = 0;
+    return cuda_fail(ssim2d_staging_status(flags_out, true));
+}
+
 size_t gbssim_workspace_bytes(int N, int C, int H, int W, int padding)
 {
     if (!shape2d_ok(N, C, H, W, padding)) return 0;
@@ -330,6 +342,7 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    ssim2d_prepare_staging(a, (long long)N * C, grad);
     a.out1 = grad ? saved_or_null : nullptr;
     a.out2 = (grad && want_grad2) ? saved_or_null + size_t(N) * C * H * W : nullptr;
     a.dL = nullptr;
@@ -398,6 +411,7 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    ssim2d_prepare_staging(a, (long long)N * C, true);
     a.out1 = grad_img1;
     a.out2 = grad_img2_or_null;
     a.dL = dL;
@@ -603,6 +617,7 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
     a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    ssim2d_prepare_staging(a, (long long)N * C, true);
     a.out1 = grad_img1;
     a.out2 = grad_img2_or_null;
     a.dL = dL;

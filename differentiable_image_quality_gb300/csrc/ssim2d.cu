@@ -34,6 +34,9 @@
 //   training forward: the gradient fields of mean[n] itself (dL = 1) go to the
 //                     caller's `saved` buffer, and the mean is reduced too;
 //   recompute backward: the fields times dL[n] go to grad_img1 / grad_img2.
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "common.cuh"
 #include "ssim2d.cuh"
 
@@ -56,6 +59,10 @@ constexpr int P1 = 132;                // float pitch of the single adjoint plan
 constexpr int CBP = 124;               // float pitch of the chain-rule pixel rows (16-byte rows)
 constexpr int CBOFF = 2;               // gradient column jj sits at cb column jj + CBOFF
 constexpr int NBUF = 2;                // input row blocks in flight
+constexpr int XB = (STEP * IWP + 31) / 32 * 32;   // float stride of a staged block (128-byte multiple)
+constexpr int CBB = (STEP * CBP + 31) / 32 * 32;  // float stride of a chain-rule pixel block
+constexpr long long kWaitCycles = 1LL << 31;      // staging wait limit (about a second)
+constexpr long long kDrainCycles = 1LL << 27;     // after a failed wait: copies still in flight
 
 static_assert(SWG <= NT, "one thread per statistic column");
 static_assert(IWP % 4 == 0 && IWP >= SW + 10 && IWP >= GW + 20, "input pitch");
@@ -67,6 +74,18 @@ static_assert((GW - GSHIFT - CBOFF) % 4 == 0 && (GSHIFT + CBOFF) % 4 == 0,
 static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
               "gradient strips stage from 16-byte aligned columns");
 
+// Tensor staging.  On the aligned path one thread issues, per row block, two
+// tensor copies (img1, img2) of STEP rows x IWP columns at (ic0, first row,
+// plane); the copy unit writes zeros for every coordinate outside the image, so
+// the halo needs no special case.  Completion is tracked by a transaction
+// barrier per buffer (and one for the chain-rule pixels); every wait on one is
+// bounded, and a block whose wait runs out stops, records the failure and
+// returns NaN as its partial sum.
+constexpr unsigned kBlockTx = 2u * STEP * IWP * sizeof(float);
+constexpr unsigned kChainTx = 2u * STEP * CBP * sizeof(float);
+
+__device__ unsigned g_staging_status;  // bit 0: a staging wait ran out of time
+
 // Staged rows start at input column ic0, a multiple of 4 in both modes (the
 // strips are shifted to make it so): then, when W % 4 == 0 and the images are
 // 16-byte aligned, whole rows move as 16-byte cp.async chunks, entirely inside
@@ -74,28 +93,36 @@ static_assert((GW - GSHIFT - 10) % 4 == 0 && (GSHIFT + 10) % 4 == 0,
 __device__ __forceinline__ int stat_shift(int off) { return (4 - (off & 3)) & 3; }
 
 // Shared memory (byte offsets):
-//   xs, ys  [NBUF][STEP][IWP] float       input rows
+//   xs, ys  [NBUF][XB] float               input rows: STEP rows of IWP floats
 //   hb      [HBUF] float4                  row-blurred statistics (m1, m2, es, e12)
 // gradient mode only:
 //   va      [STEP][P2] float2              adjoint column sums (g_m1, g_e)
 //   vb2     [STEP][P2] float2              (g_e12, g_m2)        [grad2]
 //   vc      [STEP][P1] float               g_e12                [grad1 only]
-//   cbx,cby [STEP][CBP] float              input pixels of this step's gradient rows
+//   cbx,cby [CBB] float                    input pixels of this step's gradient rows,
+//                                          STEP rows of CBP floats
+// Every buffer starts on a 128-byte boundary (tensor-copy destinations).
 // Work items of the row passes are numbered row-fastest (item = g * STEP + k),
 // so the eight threads of a quarter warp mostly touch eight consecutive rows;
 // the odd pitches (in 16-byte units: IWP 35, RP 129, P2 65, P1 33) put those in
 // distinct bank groups, and every address inside an item is a base plus a
 // compile-time offset.
-constexpr size_t kInBytes = size_t(2) * NBUF * STEP * IWP * sizeof(float);
-constexpr size_t kHbBytes = size_t(HBUF) * sizeof(float4);
-constexpr size_t kPairPlane = size_t(STEP) * P2 * sizeof(float2);
-constexpr size_t kOnePlane = size_t(STEP) * P1 * sizeof(float);
-constexpr size_t kCbBytes = size_t(2) * STEP * CBP * sizeof(float);
+constexpr size_t round128(size_t b) { return (b + 127) / 128 * 128; }
+constexpr size_t kInBytes = size_t(2) * NBUF * XB * sizeof(float);
+constexpr size_t kHbBytes = round128(size_t(HBUF) * sizeof(float4));
+constexpr size_t kPairPlane = round128(size_t(STEP) * P2 * sizeof(float2));
+constexpr size_t kOnePlane = round128(size_t(STEP) * P1 * sizeof(float));
+constexpr size_t kCbBytes = size_t(2) * CBB * sizeof(float);
 
+// Dynamic shared memory, plus 128 bytes to align its base.
 __host__ __device__ constexpr size_t smem_bytes_for(bool grad, bool g2)
 {
-    return kInBytes + kHbBytes + (grad ? kPairPlane + (g2 ? kPairPlane : kOnePlane) + kCbBytes : 0);
+    return 128 + kInBytes + kHbBytes +
+           (grad ? kPairPlane + (g2 ? kPairPlane : kOnePlane) + kCbBytes : 0);
 }
+// Three gradient CTAs per SM: 228 KB per SM, 1 KB reserved per CTA, ~0.2 KB static.
+static_assert(3 * (smem_bytes_for(true, false) + 1024 + 256) <= 233472,
+              "three grad_img1 CTAs fit in an SM's shared memory");
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
@@ -131,23 +158,26 @@ template <bool GRAD, bool G2>
 constexpr int min_blocks() { return (GRAD && G2) ? 2 : 3; }
 
 template <bool GRAD, bool G2>
-__global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kernel(const Ssim2dArgs a)
+__global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
+    ssim2d_stream_kernel(const __grid_constant__ Ssim2dArgs a)
 {
     constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
     constexpr int NGH = SW / KH;
     static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_dyn[];
+    unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
     float *xs = reinterpret_cast<float *>(smem_raw);
-    float *ys = xs + NBUF * STEP * IWP;
+    float *ys = xs + NBUF * XB;
     float4 *hb = reinterpret_cast<float4 *>(smem_raw + kInBytes);
     unsigned char *gbase = smem_raw + kInBytes + kHbBytes;
     float2 *va = reinterpret_cast<float2 *>(gbase);
     float2 *vb2 = reinterpret_cast<float2 *>(gbase + kPairPlane);
     float *vc = reinterpret_cast<float *>(gbase + kPairPlane);
     float *cbx = reinterpret_cast<float *>(gbase + kPairPlane + (G2 ? kPairPlane : kOnePlane));
-    float *cby = cbx + STEP * CBP;
+    float *cby = cbx + CBB;
     __shared__ double red[NT / 32];
+    __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
     const int tid = threadIdx.x;
     int bidx = blockIdx.x;
@@ -192,20 +222,28 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     auto load_block = [&](int t) {
         const int buf = t % NBUF;
         const int rbase = R0 + t * STEP;
+        if (a.tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars[buf], kBlockTx + a.tx_extra);
+                tma_load_3d(xs + buf * XB, &a.tm_x, ic0, rbase, plane, &bars[buf]);
+                tma_load_3d(ys + buf * XB, &a.tm_y, ic0, rbase, plane, &bars[buf]);
+            }
+            return;
+        }
         if (a.vec16) {
             for (int e = tid; e < STEP * NCHK; e += NT) {
                 const int ri = e / NCHK, ch = e - ri * NCHK;
                 const int R = rbase + ri, Cc = ic0 + 4 * ch;
                 const bool inb = (R >= 0) && (R < a.H) && (Cc >= 0) && (Cc < a.W);
                 const size_t gi = inb ? size_t(R) * a.W + Cc : 0;
-                const int si = (buf * STEP + ri) * IWP + 4 * ch;
+                const int si = buf * XB + ri * IWP + 4 * ch;
                 cp_async16(xs + si, xp + gi, inb);
                 cp_async16(ys + si, yp + gi, inb);
             }
             return;
         }
-        float *dx = xs + buf * STEP * IWP + tid;
-        float *dy = ys + buf * STEP * IWP + tid;
+        float *dx = xs + buf * XB + tid;
+        float *dy = ys + buf * XB + tid;
 #pragma unroll
         for (int ri = 0; ri < STEP; ++ri) {
             const int R = rbase + ri;
@@ -228,6 +266,14 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     //      gradient columns jj at cb column jj + CBOFF (zeros outside the image)
     auto load_chain = [&](int t) {
         const int qb = R0 + t * STEP - 10;
+        if (a.tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars[2], kChainTx + a.tx_extra);
+                tma_load_3d(cbx, &a.tm_cx, j0 - CBOFF, qb, plane, &bars[2]);
+                tma_load_3d(cby, &a.tm_cy, j0 - CBOFF, qb, plane, &bars[2]);
+            }
+            return;
+        }
         if (a.vec16) {
             // 16-byte chunks from column j0 - CBOFF (a multiple of 4): each chunk
             // entirely inside or outside the image (W % 4 == 0)
@@ -258,7 +304,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     // ---- row pass of the statistics: row k of block t, columns [KH g, KH g + KH)
     auto h_item = [&](int t, int item) {
         const int g = item / STEP, k = item - g * STEP;
-        const int base = ((t % NBUF) * STEP + k) * IWP + g * KH;  // float4-aligned
+        const int base = (t % NBUF) * XB + k * IWP + g * KH;  // float4-aligned
         float xv[KH + 10], yv[KH + 10];
 #pragma unroll
         for (int m = 0; m < KH + 8; m += 4) {
@@ -419,15 +465,36 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
     int klo = 0, khi = 0, kown = 0;  // rows k of the current step: valid in [klo, khi), owned from kown
 
     // ---- prologue
+    if (a.tma) {
+        if (tid == 0) {
+            mbar_init(&bars[0], 1);
+            mbar_init(&bars[1], 1);
+            mbar_init(&bars[2], 1);
+            mbar_init_fence();
+        }
+        __syncthreads();
+    }
+    int issued_blocks = 0, issued_chains = 0;  // tensor copies issued (uniform)
     load_block(0);
-    if (GRAD) load_chain(0);
+    ++issued_blocks;
+    if (GRAD) {
+        load_chain(0);
+        ++issued_chains;
+    }
     cp_async_commit();
-    if (steps > 1) load_block(1);
+    if (steps > 1) {
+        load_block(1);
+        ++issued_blocks;
+    }
     cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int i = tid; i < STEP * NGH; i += NT) h_item(0, i);
-    __syncthreads();
+    bool ok = true;
+    if (a.tma) ok = mbar_wait_bounded(&bars[0], 0, kWaitCycles);
+    else cp_async_wait<0>();
+    bool failed = __syncthreads_or(!ok);
+    if (!failed) {
+        for (int i = tid; i < STEP * NGH; i += NT) h_item(0, i);
+        __syncthreads();
+    }
 
     auto v_row = [&](auto K_, int t) {
         constexpr int k = decltype(K_)::value;
@@ -467,7 +534,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         }
     };
 
-    for (int t = 0; t < steps; ++t) {
+    for (int t = 0; t < steps && !failed; ++t) {
         // rows of this step: r = rb + k, statistic row p = r + off - 10
         const int rb = R0 + t * STEP;
         const int pb = rb + a.off - 10;
@@ -486,8 +553,17 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         v_row(std::integral_constant<int, 8>{}, t);
         v_row(std::integral_constant<int, 9>{}, t);
         v_row(std::integral_constant<int, 10>{}, t);
-        cp_async_wait<0>();  // block t+1 and the chain-rule pixels of step t have landed
-        __syncthreads();
+        // block t+1 and the chain-rule pixels of step t have landed
+        if (a.tma) {
+            ok = (t + 1 >= steps) || mbar_wait_bounded(&bars[(t + 1) & 1], ((t + 1) >> 1) & 1, kWaitCycles);
+            if (GRAD && ok) ok = mbar_wait_bounded(&bars[2], t & 1, kWaitCycles);
+        } else {
+            cp_async_wait<0>();
+        }
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
         // ---- H of step t+1 and A of step t.  The row-pass items are counted in
         //      whole warps (NHP) so that no warp runs both kinds in one round.
         constexpr int NHP = (STEP * NGH + 31) / 32 * 32;
@@ -503,15 +579,31 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>()) ssim2d_stream_kern
         }
         __syncthreads();
         // block t's buffer (read by H(t) long ago) and cb (just read by A(t)) are free
-        if (t + 2 < steps) load_block(t + 2);
-        if (GRAD && t + 1 < steps) load_chain(t + 1);
+        if (t + 2 < steps) {
+            load_block(t + 2);
+            ++issued_blocks;
+        }
+        if (GRAD && t + 1 < steps) {
+            load_chain(t + 1);
+            ++issued_chains;
+        }
         cp_async_commit();
     }
     cp_async_wait<0>();
+    if (failed && tid == 0) {
+        // let the tensor copies still in flight land (bounded), then record the failure
+        const long long t0 = clock64();
+        for (int b = 0; b < 3; ++b) {
+            const int n = b < 2 ? (issued_blocks + 1 - b) / 2 : issued_chains;
+            const long long left = kDrainCycles - (clock64() - t0);
+            if (n > 0 && left > 0) mbar_wait_bounded(&bars[b], (n - 1) & 1, left);
+        }
+        atomicOr(&g_staging_status, 1u);
+    }
 
     if (want_mean) {
         const double tot = block_sum<NT>(ssum, red);
-        if (tid == 0) a.partials[blockIdx.x] = tot;
+        if (tid == 0) a.partials[blockIdx.x] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
         finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
     }
 }
@@ -554,6 +646,39 @@ __global__ void __launch_bounds__(256) scale_fields_scalar(const float *f1, cons
 
 size_t smem_bytes(bool grad, bool g2) { return smem_bytes_for(grad, g2); }
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// [planes][H][W] float32 at ptr; box of `rows` rows x `cols` columns of one plane;
+// out-of-range elements read as zeros.
+bool encode_rows_map(CUtensorMap &m, const float *ptr, long long planes, int H, int W, int cols,
+                     int rows)
+{
+    const auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(W), cuuint64_t(H), cuuint64_t(planes)};
+    const cuuint64_t strides[2] = {cuuint64_t(W) * sizeof(float),
+                                   cuuint64_t(H) * cuuint64_t(W) * sizeof(float)};
+    const cuuint32_t box[3] = {cuuint32_t(cols), cuuint32_t(rows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool GRAD, bool G2>
 cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
 {
@@ -564,6 +689,35 @@ cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
 }  // namespace
 
 size_t ssim2d_smem_bytes(bool grad, bool g2) { return smem_bytes(grad, g2); }
+
+int g_staging_mode = 0;
+
+void ssim2d_prepare_staging(Ssim2dArgs &a, long long planes, bool grad)
+{
+    // the maps need 16-byte aligned bases and row pitches (a.vec16) and strides
+    // below 2^40 bytes
+    const unsigned long long plane_bytes = (unsigned long long)a.H * a.W * sizeof(float);
+    bool ok = g_staging_mode != 1 && a.vec16 && plane_bytes < (1ULL << 40) && planes < (1LL << 31);
+    ok = ok && encode_rows_map(a.tm_x, a.x, planes, a.H, a.W, IWP, STEP) &&
+         encode_rows_map(a.tm_y, a.y, planes, a.H, a.W, IWP, STEP);
+    if (ok && grad)
+        ok = encode_rows_map(a.tm_cx, a.x, planes, a.H, a.W, CBP, STEP) &&
+             encode_rows_map(a.tm_cy, a.y, planes, a.H, a.W, CBP, STEP);
+    a.tma = ok ? 1 : 0;
+    a.tx_extra = (ok && g_staging_mode == 2) ? 16u : 0u;
+}
+
+void ssim2d_set_staging_mode(int mode) { g_staging_mode = (mode >= 0 && mode <= 2) ? mode : 0; }
+
+cudaError_t ssim2d_staging_status(unsigned *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_staging_status, sizeof(unsigned));
+    if (e == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_staging_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
 
 int ssim2d_strips(bool grad, int W, int Wo, int off)
 {

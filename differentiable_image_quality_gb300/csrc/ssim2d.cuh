@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gbssim {
@@ -10,7 +11,13 @@ constexpr int kThreads2d = 128;
 
 // Arguments of the 2D streaming kernel.  The grid is one block per
 // (plane, row segment, column strip), flattened with the strip fastest.
+// Passed as a grid constant: the tensor maps are read in place.
 struct Ssim2dArgs {
+    // tensor staging (tma = 1): maps of img1 / img2 as [planes][H][W] with the
+    // boxes of a staged row block and of a block of chain-rule pixel rows
+    CUtensorMap tm_x, tm_y, tm_cx, tm_cy;
+    int tma;
+    unsigned tx_extra;  // test hook: bytes announced beyond the copies (0)
     const float *x;  // img1 [planes, H, W]
     const float *y;  // img2
     int H, W;        // input extent
@@ -33,6 +40,16 @@ struct Ssim2dArgs {
 };
 
 size_t ssim2d_smem_bytes(bool grad, bool g2);
+// Tensor maps of the staging copies for a.x / a.y ([planes][H][W]); sets a.tma to
+// 1 when every map was encoded (a.vec16 required), else 0 (cp.async staging).
+void ssim2d_prepare_staging(Ssim2dArgs &a, long long planes, bool grad);
+// Reads (and with clear, resets) the device's record of staging waits that ran
+// out of time (bit 0).  Synchronous.
+cudaError_t ssim2d_staging_status(unsigned *flags, bool clear);
+// Staging mode: 0 tensor copies where possible, 1 cp.async only, 2 tensor copies
+// that announce 16 bytes more than they deliver, so that every wait runs out
+// (test of the failure path).
+void ssim2d_set_staging_mode(int mode);
 // Column strips of a plane in gradient mode (over W) or forward-only mode (over Wo).
 int ssim2d_strips(bool grad, int W, int Wo, int off);
 const void *ssim2d_kernel_ptr(bool grad, bool g2);

@@ -66,6 +66,17 @@ const char *gbssim_strerror(int status);
  * float32 roundings of exp(-(k-5)^2 / 4.5), k = 0..10, divided by their sum. */
 void gbssim_window(float w[11]);
 
+/* Kernel-side failures recorded on the current device since the previous call,
+ * as bit flags in *flags_out, which this call then clears.
+ *   bit 0 (GBSSIM_DEV_STAGING_TIMEOUT): a 2D kernel waited about a second for
+ *   its staged input rows without them arriving; its blocks stopped early, so
+ *   that call's gradients and map are not valid, and the mean of each image
+ *   with a stopped block is NaN.
+ * Synchronises the device: a diagnostic, not part of the hot path.  Returns
+ * GBSSIM_OK, GBSSIM_EINVAL (null flags_out) or GBSSIM_ECUDA. */
+#define GBSSIM_DEV_STAGING_TIMEOUT 1u
+int gbssim_device_status(unsigned *flags_out);
+
 /* ------------------------------------------------------------------ 2D ----- */
 
 /* Bytes of scratch that ssim_fwd needs for the given shape (per-block partial

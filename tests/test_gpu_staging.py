@@ -1,0 +1,96 @@
+"""The two ways the 2D kernels stage input rows, and the bounded staging wait.
+
+On 16-byte aligned images with W % 4 == 0 the kernels stage rows with tensor
+copies (one thread per block issues them; a transaction barrier tracks them);
+otherwise, or when the staging hook asks for it, every thread issues cp.async
+copies.  Both must give the oracle's results.  A wait for a tensor copy is
+bounded: when it runs out, the kernel's blocks stop, the device records the
+failure, the affected means come out NaN, and the context stays usable.  The
+hook's mode 2 makes every wait run out by announcing 16 bytes more than the
+copies deliver; no fault is involved.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from test_gpu_parity import _assert_parity, _oracle, _run
+from workloads import dl_vector, make_inputs, uniform_pair
+
+pytestmark = pytest.mark.gpu
+
+STAGING_TIMEOUT = 1  # GBSSIM_DEV_STAGING_TIMEOUT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from differentiable_image_quality_gb300 import _abi, _build
+
+    _build.build()
+    return _abi.load()
+
+
+def _status(lib):
+    flags = ctypes.c_uint(0xFFFFFFFF)
+    assert lib.gbssim_device_status(ctypes.byref(flags)) == 0
+    return flags.value
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape,padding", [((1, 3, 64, 64), "valid"), ((1, 3, 64, 64), "same"),
+                                           ((2, 1, 129, 12), "valid"),
+                                           ((1, 2, 130, 236), "same"),
+                                           ((1, 1, 75, 500), "valid")])
+def test_both_staging_paths_match_the_oracle(lib, oracle_mod, shape, padding, mode):
+    import torch
+
+    x, y = uniform_pair(shape, 950 + shape[3], std=0.08)
+    dl = np.linspace(-1.0, 0.5, shape[0])
+    ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
+    lib.gbssim_tune_staging(mode)
+    try:
+        for path in ("saved", "recompute"):
+            got = _run(torch.device("cuda:0"), x, y, dl, padding, True, path, want_map=True)
+            _assert_parity(got, ref, True, f"mode {mode} {shape} {padding} {path}")
+    finally:
+        lib.gbssim_tune_staging(0)
+
+
+def test_cp_async_staging_on_the_1080p_pair(lib, oracle_mod):
+    import torch
+
+    x, y = make_inputs("splat1080_valid")
+    dl = dl_vector("splat1080_valid")
+    ref = _oracle(oracle_mod, x, y, dl, "valid", False)
+    lib.gbssim_tune_staging(1)
+    try:
+        got = _run(torch.device("cuda:0"), x, y, dl, "valid", False, "saved")
+    finally:
+        lib.gbssim_tune_staging(0)
+    _assert_parity(got, ref, False, "cp.async staging, 1080p")
+
+
+def test_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
+    import torch
+
+    dev = torch.device("cuda:0")
+    assert _status(lib) == 0, "an earlier call recorded a staging timeout"
+    x, y = uniform_pair((2, 1, 64, 64), 990, std=0.08)
+    dl = np.array([-1.0, 0.5])
+    lib.gbssim_tune_staging(2)
+    try:
+        stalled = _run(dev, x, y, dl, "valid", False, "saved")
+    finally:
+        lib.gbssim_tune_staging(0)
+    assert _status(lib) & STAGING_TIMEOUT
+    assert np.all(np.isnan(stalled["mean"]))
+    assert _status(lib) == 0  # reading the status cleared it
+    # the same call without the stall, on the same context
+    got = _run(dev, x, y, dl, "valid", False, "saved")
+    ref = _oracle(oracle_mod, x, y, dl, "valid", False)
+    _assert_parity(got, ref, False, "after a staging timeout")
+    assert _status(lib) == 0
