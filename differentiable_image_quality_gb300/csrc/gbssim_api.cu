@@ -1,8 +1,10 @@
 // The C ABI (include/gbssim.h): argument checks, launch planning, dispatch.
 // Host code only; every step of the computation runs in the kernels.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "gbssim.h"
 #include "common.cuh"
@@ -91,10 +93,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// Launch plan of the 2D streaming kernel: column strips x row segments x planes.
+// Launch plan of the 2D streaming kernel: per plane, `per_plane` blocks over the
+// column strips; strips [0, extra) get base + 1 row segments, the rest base.
 struct Plan2d {
-    int strips = 0, segs = 0, seg_rows = 0;
-    long long blocks = 0;
+    int strips = 0, per_plane = 0, base = 0, extra = 0;
+    long long blocks = 0, long_blocks = 0;
 };
 
 // Relative SM throughput with k resident CTAs (k = 1, 2, 3, 4+), measured on the
@@ -105,10 +108,10 @@ double occupancy_eff(int k)
     return e[k < 1 ? 0 : (k > 4 ? 3 : k - 1)];
 }
 
-// Time of `blocks` CTAs of `steps` row steps each, in units of one CTA-step at
-// full occupancy: the grid runs in waves of SMs x occ CTAs; a wave whose
-// busiest SM holds k CTAs takes k (steps + 1) / eff(k) (the +1 is a CTA's fixed
-// start-up and finish).
+// Time of `blocks` equal CTAs of `steps` row steps each, in units of one
+// CTA-step at full occupancy: the grid runs in waves of SMs x occ CTAs; a wave
+// whose busiest SM holds k CTAs takes k (steps + 1) / eff(k) (the +1 is a CTA's
+// fixed start-up and finish).
 double wave_cost(long long blocks, long long steps, int sm_count, int occ)
 {
     const long long slots = (long long)sm_count * occ;
@@ -122,37 +125,96 @@ double wave_cost(long long blocks, long long steps, int sm_count, int occ)
     return cost;
 }
 
-// Pick the row segmentation: a gradient-mode segment walks seg_rows + 20 input
-// rows, a forward-only one seg_rows + 10.
+// Same units for CTAs of two lengths that fit in one wave (blocks <= SMs x occ):
+// the long ones are issued first, one per SM in turn, then each short one goes
+// to the least loaded SM (the block scheduler fills free slots in order).
+double one_wave_cost(long long n_long, long long s_long, long long n_short, long long s_short,
+                     int sm_count)
+{
+    std::vector<long long> load(size_t(sm_count), 0), cnt(size_t(sm_count), 0);
+    for (long long i = 0; i < n_long; ++i) {
+        load[size_t(i % sm_count)] += s_long + 1;
+        ++cnt[size_t(i % sm_count)];
+    }
+    for (long long i = 0; i < n_short; ++i) {
+        size_t m = 0;
+        for (size_t j = 1; j < load.size(); ++j)
+            if (load[j] < load[m]) m = j;
+        load[m] += s_short + 1;
+        ++cnt[m];
+    }
+    double worst = 0.0;
+    for (size_t j = 0; j < load.size(); ++j)
+        if (cnt[j]) worst = std::max(worst, double(load[j]) / occupancy_eff(int(cnt[j])));
+    return worst;
+}
+
+long long seg_steps(int rows, int nseg, int halo)
+{
+    return ceil_div(ceil_div(rows, nseg) + halo, kTaps);
+}
+
+// Pick the segmentation.  Candidates: every strip with s segments (s = 1 ..
+// rows / kMinSegRows), costed by the wave model; and the largest per-plane count
+// that still fits one wave, with the strips' segment counts differing by one
+// (the last strip of a plane, usually the narrowest, gets the fewer), costed by
+// one_wave_cost.  A gradient-mode segment walks its rows + 20, a forward-only
+// one its rows + 10.
 Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad, int sm_count,
               int occ)
 {
     Plan2d p;
     const int rows = grad ? H : Ho;
     const int halo = grad ? 20 : 10;
-    p.strips = ssim2d_strips(grad, W, Wo, off);
-    const long long cols_planes = (long long)p.strips * planes;
-    const int max_segs = int(ceil_div(rows, kMinSegRows));
+    const int S = ssim2d_strips(grad, W, Wo, off);
+    p.strips = S;
+    const int max_segs = std::max(1, rows / kMinSegRows);
+    auto take = [&](int per_plane) {
+        p.per_plane = per_plane;
+        p.base = per_plane / S;
+        p.extra = per_plane % S;
+        p.blocks = planes * per_plane;
+        p.long_blocks = planes * (S - p.extra) * p.base;
+    };
+    if (g_seg_rows_override > 0) {
+        take(S * int(ceil_div(rows, std::min(g_seg_rows_override, rows))));
+        return p;
+    }
     double best = -1.0;
     long long best_work = 0;
+    int best_k = S;
     for (int s = 1; s <= max_segs; ++s) {
-        int sr = int(ceil_div(rows, s));
-        if (g_seg_rows_override > 0) sr = g_seg_rows_override < rows ? g_seg_rows_override : rows;
-        const int segs = int(ceil_div(rows, sr));
-        const long long blocks = cols_planes * segs;
-        const long long steps = ceil_div(sr + halo, kTaps);
+        const long long blocks = (long long)S * planes * s;
+        const long long steps = seg_steps(rows, s, halo);
         const double cost = wave_cost(blocks, steps, sm_count, occ);
         const long long work = blocks * steps;
         if (best < 0 || cost < best - 1e-9 || (cost <= best + 1e-9 && work < best_work)) {
             best = cost;
             best_work = work;
-            p.segs = segs;
-            p.seg_rows = sr;
-            p.blocks = blocks;
+            best_k = S * s;
         }
-        if (g_seg_rows_override > 0) break;
     }
+    const long long slots = (long long)sm_count * occ;
+    const long long fill = slots / planes;  // blocks per plane that fill one wave
+    if (fill > S && fill < (long long)S * max_segs && fill % S != 0) {
+        const int k = int(fill), base = k / S, extra = k % S;
+        const double cost = one_wave_cost(planes * (S - extra) * base, seg_steps(rows, base, halo),
+                                          planes * extra * (base + 1),
+                                          seg_steps(rows, base + 1, halo), sm_count);
+        if (cost < best - 1e-9) best_k = k;
+    }
+    take(best_k);
     return p;
+}
+
+void set_segments(Ssim2dArgs &a, const Plan2d &p, int rows)
+{
+    a.strips = p.strips;
+    a.rows = rows;
+    a.per_plane = p.per_plane;
+    a.seg_base = p.base;
+    a.seg_extra = p.extra;
+    a.long_blocks = int(p.long_blocks);
 }
 
 // Upper bound of blocks over every plan (segments never shorter than kMinSegRows).
@@ -268,9 +330,9 @@ void gbssim_window(float w[11])
     for (int k = 0; k < kTaps; ++k) w[k] = tap(k);
 }
 
-// Tuning hook for benchmarks: force the row-segment length of the 2D planner
-// (0 restores the planner; lengths below the planner's minimum are raised to
-// it).  Results do not depend on it.
+// Tuning hook for benchmarks: make the 2D planner cut every strip into
+// ceil(rows / `rows`) equal row segments (0 restores the planner; lengths below
+// the planner's minimum are raised to it).  Results do not depend on it.
 void gbssim_tune_seg_rows(int rows)
 {
     g_seg_rows_override = rows > 0 ? (rows < kMinSegRows ? kMinSegRows : rows) : 0;
@@ -339,7 +401,7 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    set_segments(a, p, grad ? H : Ho);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, grad);
@@ -408,7 +470,7 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    set_segments(a, p, H);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, true);
@@ -614,7 +676,7 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    a.strips = p.strips; a.segs = p.segs; a.seg_rows = p.seg_rows;
+    set_segments(a, p, H);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, true);

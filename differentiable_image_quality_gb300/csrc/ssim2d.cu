@@ -152,6 +152,44 @@ __device__ __forceinline__ float ring_sum1(const float (&r)[kTaps])
     return acc;
 }
 
+// The work of block b.  Each plane has `per_plane` blocks over its column strips:
+// strips [0, seg_extra) are cut into seg_base + 1 row segments, the others into
+// seg_base (the rows split as evenly as integers allow).  Blocks are numbered
+// longest segments first (all planes), then the shorter ones, so that the block
+// scheduler starts the long ones first and spreads them over the SMs.  `slot`
+// numbers the blocks plane by plane: the partial sums of one image are contiguous.
+struct SegWork {
+    int plane, strip, seg, r0, r1, slot;
+};
+
+__device__ __forceinline__ SegWork segment_of(const Ssim2dArgs &a, int b)
+{
+    const int base = a.seg_base, extra = a.seg_extra;
+    const int nl = (a.strips - extra) * base;  // blocks with base segments, per plane
+    const int ns = extra * (base + 1);         // blocks with base + 1 segments, per plane
+    SegWork w;
+    int r, nseg;
+    if (b < a.long_blocks) {
+        w.plane = b / nl;
+        r = b - w.plane * nl;
+        w.strip = extra + r / base;
+        w.seg = r - (w.strip - extra) * base;
+        nseg = base;
+        w.slot = w.plane * a.per_plane + ns + r;
+    } else {
+        const int b2 = b - a.long_blocks;
+        w.plane = b2 / ns;
+        r = b2 - w.plane * ns;
+        w.strip = r / (base + 1);
+        w.seg = r - w.strip * (base + 1);
+        nseg = base + 1;
+        w.slot = w.plane * a.per_plane + r;
+    }
+    w.r0 = int((long long)w.seg * a.rows / nseg);
+    w.r1 = int((long long)(w.seg + 1) * a.rows / nseg);
+    return w;
+}
+
 // Resident CTAs per SM the kernel is built for: three for the forward-only and
 // the grad_img1 kernels (75 KB of shared memory, <= 168 registers), two with grad_img2.
 template <bool GRAD, bool G2>
@@ -180,11 +218,8 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
     const int tid = threadIdx.x;
-    int bidx = blockIdx.x;
-    const int strip = bidx % a.strips;
-    bidx /= a.strips;
-    const int seg = bidx % a.segs;
-    const int plane = bidx / a.segs;
+    const SegWork w = segment_of(a, blockIdx.x);
+    const int strip = w.strip, seg = w.seg, plane = w.plane;
     const int n = plane / a.C;
     const size_t plane_off = size_t(plane) * size_t(a.H) * size_t(a.W);
     const float *__restrict__ xp = a.x + plane_off;
@@ -195,16 +230,15 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     int j0 = 0, sc0, ic0, R0, nrows, q0 = 0, q1 = 0;
     if (GRAD) {
         j0 = strip * GW - GSHIFT;
-        q0 = seg * a.seg_rows;
-        q1 = min(q0 + a.seg_rows, a.H);
+        q0 = w.r0;
+        q1 = w.r1;
         sc0 = j0 + a.off - 10;
         ic0 = j0 - 10;
         R0 = q0 - 10;
         nrows = q1 - q0 + 20;
     } else {
         sc0 = strip * SW - stat_shift(a.off);
-        const int r0 = seg * a.seg_rows;
-        const int r1 = min(r0 + a.seg_rows, a.Ho);
+        const int r0 = w.r0, r1 = w.r1;
         ic0 = sc0 - a.off;
         R0 = r0 - a.off;
         nrows = r1 - r0 + 10;
@@ -603,7 +637,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
 
     if (want_mean) {
         const double tot = block_sum<NT>(ssum, red);
-        if (tid == 0) a.partials[blockIdx.x] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
+        if (tid == 0) a.partials[w.slot] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
         finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
     }
 }

@@ -9,8 +9,8 @@ namespace gbssim {
 
 constexpr int kThreads2d = 128;
 
-// Arguments of the 2D streaming kernel.  The grid is one block per
-// (plane, row segment, column strip), flattened with the strip fastest.
+// Arguments of the 2D streaming kernel.  The grid is one block per (plane,
+// column strip, row segment); strips may have different numbers of segments.
 // Passed as a grid constant: the tensor maps are read in place.
 struct Ssim2dArgs {
     // tensor staging (tma = 1): maps of img1 / img2 as [planes][H][W] with the
@@ -24,7 +24,9 @@ struct Ssim2dArgs {
     int Ho, Wo;      // output-domain extent (valid: H-10, W-10; same: H, W)
     int off;         // window offset: 0 valid, 5 same
     int C;           // channels (plane / C = image index)
-    int strips, segs, seg_rows;
+    // segmentation (see segment_of): rows = H (gradient mode) or Ho; per_plane
+    // blocks per plane; long_blocks = planes * (strips - seg_extra) * seg_base
+    int strips, rows, per_plane, seg_base, seg_extra, long_blocks;
     int vec16;       // 1: W % 4 == 0 and x, y 16-byte aligned (16-byte staging)
     // gradient mode: fields written here (grad of mean[n] * dL[n]); out2 may be null
     float *out1, *out2;
