@@ -4,6 +4,7 @@
 #include <climits>
 #include <cstdint>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "gbssim.h"
@@ -136,12 +137,16 @@ double one_wave_cost(long long n_long, long long s_long, long long n_short, long
         load[size_t(i % sm_count)] += s_long + 1;
         ++cnt[size_t(i % sm_count)];
     }
+    // (load, SM) min-heap: ties go to the lower-numbered SM
+    using Entry = std::pair<long long, int>;
+    std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> heap;
+    for (int j = 0; j < sm_count; ++j) heap.push({load[size_t(j)], j});
     for (long long i = 0; i < n_short; ++i) {
-        size_t m = 0;
-        for (size_t j = 1; j < load.size(); ++j)
-            if (load[j] < load[m]) m = j;
-        load[m] += s_short + 1;
-        ++cnt[m];
+        const Entry e = heap.top();
+        heap.pop();
+        load[size_t(e.second)] += s_short + 1;
+        ++cnt[size_t(e.second)];
+        heap.push({load[size_t(e.second)], e.second});
     }
     double worst = 0.0;
     for (size_t j = 0; j < load.size(); ++j)
@@ -204,6 +209,42 @@ Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad
         if (cost < best - 1e-9) best_k = k;
     }
     take(best_k);
+    return p;
+}
+
+// The planner's results for recent shapes (it runs a small simulation): a
+// direct-mapped cache keyed by everything plan2d reads.
+struct PlanKey {
+    long long planes;
+    int H, W, Ho, Wo, off, grad, sm_count, occ, override_rows;
+    bool operator==(const PlanKey &o) const
+    {
+        return planes == o.planes && H == o.H && W == o.W && Ho == o.Ho && Wo == o.Wo &&
+               off == o.off && grad == o.grad && sm_count == o.sm_count && occ == o.occ &&
+               override_rows == o.override_rows;
+    }
+};
+
+Plan2d cached_plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad,
+                     int sm_count, int occ)
+{
+    constexpr int kSlots = 32;
+    static PlanKey keys[kSlots];
+    static Plan2d plans[kSlots];
+    static bool used[kSlots] = {};
+    static std::mutex m;
+    const PlanKey k{planes, H, W, Ho, Wo, off, grad ? 1 : 0, sm_count, occ, g_seg_rows_override};
+    const size_t h = (size_t(planes) * 1000003u + size_t(H) * 10007u + size_t(W) * 101u +
+                      size_t(off) * 7u + size_t(grad) * 3u + size_t(occ)) % kSlots;
+    {
+        std::lock_guard<std::mutex> lock(m);
+        if (used[h] && keys[h] == k) return plans[h];
+    }
+    const Plan2d p = plan2d(planes, H, W, Ho, Wo, off, grad, sm_count, occ);
+    std::lock_guard<std::mutex> lock(m);
+    keys[h] = k;
+    plans[h] = p;
+    used[h] = true;
     return p;
 }
 
@@ -391,7 +432,7 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     if ((rc = device_info(&d))) return rc;
     const int occ = d->occ2d[grad ? (want_grad2 ? 2 : 1) : 0];
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, grad, d->sm_count, occ);
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, grad, d->sm_count, occ);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
         return GBSSIM_EWORKSPACE;
@@ -463,7 +504,7 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
                                              size_t(C) * H * W, total, d->sm_count, s));
     const int occ = d->occ2d[g2 ? 2 : 1];
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count, occ);
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count, occ);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
@@ -666,7 +707,7 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
     DeviceInfo *d = nullptr;
     if ((rc = device_info(&d))) return rc;
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
                             d->occ2d[g2 ? 2 : 1]);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))

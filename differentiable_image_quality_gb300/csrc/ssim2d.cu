@@ -496,6 +496,20 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     const bool col_own = GRAD ? (tid >= 10 || strip == 0) : true;
     const bool want_mean = (a.partials != nullptr);
     float ssum = 0.0f;
+    // Columns the strip needs (the last strip of a plane is usually narrower):
+    // statistic columns tid < nstat, gradient columns jj < ngrad.  Row-pass
+    // groups and column-pass warps wholly beyond them are skipped; the entries
+    // they would have written stay at the zeros set below.
+    const int nstat = max(0, min(GRAD ? SWG : SW, a.Wo - sc0));
+    const int ngrad = GRAD ? max(0, min(GW, a.W - j0)) : 0;
+    const int ngh = min(NGH, (nstat + KH - 1) / KH);
+    const int nga = min(NGA, (ngrad + KA - 1) / KA);
+    const bool v_warp = (tid & ~31) < nstat;
+    if (ngh < NGH || (GRAD && nga < NGA)) {
+        // hb and the adjoint planes are contiguous
+        constexpr int n4 = int((kHbBytes + (GRAD ? kPairPlane + (G2 ? kPairPlane : kOnePlane) : 0)) / 16);
+        for (int i = tid; i < n4; i += NT) hb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int klo = 0, khi = 0, kown = 0;  // rows k of the current step: valid in [klo, khi), owned from kown
 
     // ---- prologue
@@ -526,7 +540,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     else cp_async_wait<0>();
     bool failed = __syncthreads_or(!ok);
     if (!failed) {
-        for (int i = tid; i < STEP * NGH; i += NT) h_item(0, i);
+        for (int i = tid; i < STEP * ngh; i += NT) h_item(0, i);
         __syncthreads();
     }
 
@@ -576,17 +590,19 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
         khi = min(min(STEP, Rend - rb), a.Ho - pb);
         kown = (GRAD && seg != 0) ? q0 + 10 - rb : 0;  // q = r - 10 >= q0
         // ---- V: column passes of step t
-        v_row(std::integral_constant<int, 0>{}, t);
-        v_row(std::integral_constant<int, 1>{}, t);
-        v_row(std::integral_constant<int, 2>{}, t);
-        v_row(std::integral_constant<int, 3>{}, t);
-        v_row(std::integral_constant<int, 4>{}, t);
-        v_row(std::integral_constant<int, 5>{}, t);
-        v_row(std::integral_constant<int, 6>{}, t);
-        v_row(std::integral_constant<int, 7>{}, t);
-        v_row(std::integral_constant<int, 8>{}, t);
-        v_row(std::integral_constant<int, 9>{}, t);
-        v_row(std::integral_constant<int, 10>{}, t);
+        if (v_warp) {
+            v_row(std::integral_constant<int, 0>{}, t);
+            v_row(std::integral_constant<int, 1>{}, t);
+            v_row(std::integral_constant<int, 2>{}, t);
+            v_row(std::integral_constant<int, 3>{}, t);
+            v_row(std::integral_constant<int, 4>{}, t);
+            v_row(std::integral_constant<int, 5>{}, t);
+            v_row(std::integral_constant<int, 6>{}, t);
+            v_row(std::integral_constant<int, 7>{}, t);
+            v_row(std::integral_constant<int, 8>{}, t);
+            v_row(std::integral_constant<int, 9>{}, t);
+            v_row(std::integral_constant<int, 10>{}, t);
+        }
         // block t+1 and the chain-rule pixels of step t have landed
         if (a.tma) {
             ok = (t + 1 >= steps) || mbar_wait_bounded(&bars[(t + 1) & 1], ((t + 1) >> 1) & 1, kWaitCycles);
@@ -599,14 +615,13 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
             break;
         }
         // ---- H of step t+1 and A of step t.  The row-pass items are counted in
-        //      whole warps (NHP) so that no warp runs both kinds in one round.
-        constexpr int NHP = (STEP * NGH + 31) / 32 * 32;
-        const int nh = (t + 1 < steps) ? NHP : 0;
-        const int na = GRAD ? STEP * NGA : 0;
+        //      whole warps so that no warp runs both kinds in one round.
+        const int nh = (t + 1 < steps) ? (STEP * ngh + 31) / 32 * 32 : 0;
+        const int na = GRAD ? STEP * nga : 0;
         a_step = t;
         for (int i = tid; i < nh + na; i += NT) {
             if (i < nh) {
-                if (i < STEP * NGH) h_item(t + 1, i);
+                if (i < STEP * ngh) h_item(t + 1, i);
             } else {
                 a_item(i - nh);
             }
