@@ -12,7 +12,9 @@ go in and come out as float64 numpy arrays; float32 inputs are widened exactly.
 Sources followed (see the C file's header for the details):
 TriSSIM README "How it works" (the five blurred quantities, the adjoint and the
 chain rule), fused-ssim README introduction, "Usage", "Constraints" and
-"3D data" (the 11-tap window, padding modes, data range, 3D).
+"3D data" (the 11-tap window, padding modes, data range, 3D); the ssimulacra2
+hand-off page's per-octave loop (a 2x downscale between octaves, then blur,
+sigma maps and error maps per octave), read for SSIM as the maps l, cs and S.
 """
 from __future__ import annotations
 
@@ -80,6 +82,8 @@ def _load():
         lib.oracle_ssim3d_grad.argtypes = [dp, dp, dp, i, i, i, i, i, i, dp, dp]
         lib.oracle_ssim3d_grad_at.argtypes = [dp, dp, dp, i, i, i, i, i, i, ctypes.c_longlong,
                                               llp, dp, dp]
+        lib.oracle_downscale2x.argtypes = [dp, i, i, dp]
+        lib.oracle_ssim2d_components.argtypes = [dp, dp, i, i, i, i, i, dp, dp, dp, dp]
         lib.oracle_ssim_point.argtypes = [ctypes.c_double] * 5 + [dp]
         lib.oracle_ssim_point.restype = ctypes.c_double
         _lib = lib
@@ -255,3 +259,61 @@ def ssim3d_grad_at(x, y, dL, padding: str, flat_idx, want_grad2: bool = True):
         idx.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), _ptr(g1), _ptr(g2))
     _check(rc, "ssim3d_grad_at")
     return g1, g2
+
+
+def downscale2x(f) -> np.ndarray:
+    """One octave down: means of 2x2 blocks, ragged edges over their in-range pixels."""
+    f = _f64(f)
+    H, W = f.shape
+    out = np.empty(((H + 1) // 2, (W + 1) // 2))
+    _check(_load().oracle_downscale2x(_ptr(f), H, W, _ptr(out)), "downscale2x")
+    return out
+
+
+def ssim2d_components(x, y, padding: str, want_maps: bool = False):
+    """Per-image means (3, N) of the luminance term l, the contrast-structure term
+    cs and S = l * cs; with want_maps also the maps (3, N, C, Ho, Wo)."""
+    x, y = _f64(x), _f64(y)
+    if x.shape != y.shape or x.ndim != 4:
+        raise ValueError("x and y must be NCHW arrays of one shape")
+    N, C, H, W = x.shape
+    means = np.empty((3, N))
+    maps = (np.empty((3, N, C, out_extent(H, padding), out_extent(W, padding)))
+            if want_maps else None)
+    _check(_load().oracle_ssim2d_components(
+        _ptr(x), _ptr(y), N, C, H, W, _pad(padding),
+        _ptr(maps[0]) if want_maps else None, _ptr(maps[1]) if want_maps else None,
+        _ptr(maps[2]) if want_maps else None, _ptr(means)), "ssim2d_components")
+    return (means, maps) if want_maps else means
+
+
+def downscale_pair(x, y):
+    """Both NCHW images one octave down (every plane with downscale2x)."""
+    x, y = _f64(x), _f64(y)
+    N, C, H, W = x.shape
+    ox = np.empty((N, C, (H + 1) // 2, (W + 1) // 2))
+    oy = np.empty_like(ox)
+    for n in range(N):
+        for c in range(C):
+            ox[n, c] = downscale2x(x[n, c])
+            oy[n, c] = downscale2x(y[n, c])
+    return ox, oy
+
+
+def ssim2d_pyramid(x, y, padding: str, octaves: int, want_maps: bool = False):
+    """Per-octave SSIM components: octave 0 is the input pair, octave o + 1 the
+    pair of octave o one level down.  Returns means (octaves, 3, N) and, with
+    want_maps, the list of per-octave maps (3, N, C, Ho, Wo)."""
+    x, y = _f64(x), _f64(y)
+    means, maps = [], []
+    for o in range(octaves):
+        if o:
+            x, y = downscale_pair(x, y)
+        r = ssim2d_components(x, y, padding, want_maps)
+        if want_maps:
+            means.append(r[0])
+            maps.append(r[1])
+        else:
+            means.append(r)
+    means = np.stack(means)
+    return (means, maps) if want_maps else means

@@ -679,3 +679,87 @@ double oracle_ssim_point(double mu1, double mu2, double e11, double e22, double 
 {
     return ssim_point(mu1, mu2, e11, e22, e12, d5);
 }
+
+/* ------------------------------------------- per-octave SSIM maps (pyramid) */
+
+/* One octave down: out(i, j) is the mean of the pixels of the 2x2 block
+ * (2i .. 2i+1, 2j .. 2j+1) that lie inside the H x W plane, so out is
+ * ceil(H/2) x ceil(W/2) and a ragged last row or column averages the one or two
+ * pixels it has.  (The ssimulacra2 hand-off page names a 2x downscale between
+ * octaves without a formula; this is the plain box mean.) */
+int oracle_downscale2x(const double *f, int H, int W, double *out)
+{
+    if (!f || !out || H < 1 || W < 1) return -1;
+    const int Hd = (H + 1) / 2, Wd = (W + 1) / 2;
+    for (int i = 0; i < Hd; ++i) {
+        for (int j = 0; j < Wd; ++j) {
+            double acc = 0.0;
+            int cnt = 0;
+            for (int a = 0; a < 2; ++a) {
+                const int r = 2 * i + a;
+                if (r >= H) continue;
+                for (int b = 0; b < 2; ++b) {
+                    const int c = 2 * j + b;
+                    if (c >= W) continue;
+                    acc += f[(size_t)r * W + c];
+                    ++cnt;
+                }
+            }
+            out[(size_t)i * Wd + j] = acc / (double)cnt;
+        }
+    }
+    return 0;
+}
+
+/* The SSIM map split into its two factors, S = l * cs with
+ *   l  = (2 mu1 mu2 + C1) / (mu1^2 + mu2^2 + C1)        (luminance)
+ *   cs = (2 sigma12 + C2) / (sigma11 + sigma22 + C2)    (contrast-structure),
+ * from the same five blurred moments as oracle_ssim2d.  Maps (each N*C*Ho*Wo,
+ * any may be NULL) receive l, cs and S; means (3*N, or NULL) receives the
+ * per-image means of l, cs and S over channels and output pixels, in that
+ * order (means[0..N) for l, [N..2N) for cs, [2N..3N) for S). */
+int oracle_ssim2d_components(const double *x, const double *y, int N, int C, int H, int W,
+                             int padding, double *l_map, double *cs_map, double *s_map,
+                             double *means)
+{
+    if (!x || !y || N < 1 || C < 1 || check_extent(H, padding) || check_extent(W, padding))
+        return -1;
+    const double C1 = c1_const(), C2 = c2_const();
+    const size_t n = (size_t)H * W;
+    const size_t no = (size_t)oracle_out_extent(H, padding) * oracle_out_extent(W, padding);
+    double *stats = malloc(5 * no * sizeof(double));
+    if (!stats) return -1;
+    for (int b = 0; b < N; ++b) {
+        double tl = 0.0, tcs = 0.0, ts = 0.0;
+        for (int c = 0; c < C; ++c) {
+            const size_t pl = (size_t)b * C + c;
+            if (plane_stats2d(x + pl * n, y + pl * n, H, W, padding, stats)) {
+                free(stats);
+                return -1;
+            }
+            for (size_t p = 0; p < no; ++p) {
+                const double mu1 = stats[p], mu2 = stats[no + p];
+                const double s11 = stats[2 * no + p] - mu1 * mu1;
+                const double s22 = stats[3 * no + p] - mu2 * mu2;
+                const double s12 = stats[4 * no + p] - mu1 * mu2;
+                const double l = (2.0 * mu1 * mu2 + C1) / (mu1 * mu1 + mu2 * mu2 + C1);
+                const double cs = (2.0 * s12 + C2) / (s11 + s22 + C2);
+                const double S = l * cs;
+                if (l_map) l_map[pl * no + p] = l;
+                if (cs_map) cs_map[pl * no + p] = cs;
+                if (s_map) s_map[pl * no + p] = S;
+                tl += l;
+                tcs += cs;
+                ts += S;
+            }
+        }
+        if (means) {
+            const double cnt = (double)C * (double)no;
+            means[b] = tl / cnt;
+            means[N + b] = tcs / cnt;
+            means[2 * N + b] = ts / cnt;
+        }
+    }
+    free(stats);
+    return 0;
+}
