@@ -399,6 +399,22 @@ def run_ours(args):
 
         ra, rb = timed(fwd_infer, bwd_recompute, args.steps, 3)
         sa, _ = timed(single_call, None, args.steps, 3)
+        pyr = {}
+        if not is3d:
+            # the per-octave stage: l, cs and S means of every octave (maps not written)
+            H, W = x.shape[2], x.shape[3]
+            octs = 0
+            while octs < 6 and min(pkg.pyramid_extents(H, W, octs + 1)[-1]) >= (
+                    11 if wl.padding == "valid" else 1):
+                octs += 1
+            pyr_means = torch.empty((octs, 3, N), device=dev)
+
+            def pyramid():
+                pkg.ssim_pyramid(tx, ty, wl.padding, octs, out_means=pyr_means)
+
+            pa, _ = timed(pyramid, None, args.steps, 3)
+            pyr = {"pyramid_octaves": octs, "pyramid_mps": mp / (statistics.mean(pa) / 1e3),
+                   "pyramid_us": 1e3 * statistics.mean(pa)}
         extras = {
             "fwd_train_mps": mp / (fwd_ms / 1e3),
             "bwd_saved_mps": mp / (bwd_ms / 1e3),
@@ -406,6 +422,7 @@ def run_ours(args):
             "bwd_recompute_mps": mp / (statistics.mean(rb) / 1e3),
             "recompute_path_fwd_bwd_mps": mp / ((statistics.mean(ra) + statistics.mean(rb)) / 1e3),
             "single_call_fwd_bwd_mps": mp / (statistics.mean(sa) / 1e3),
+            **pyr,
         }
 
     if rank != 0:

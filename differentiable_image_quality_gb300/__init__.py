@@ -20,6 +20,12 @@ train=False is the inference mode (and a later backward recomputes).
 
 The thin wrappers ssim_fwd / ssim_bwd / ssim3d_fwd / ssim3d_bwd expose the C
 ABI calls one to one on torch tensors.
+
+    ssim_pyramid(img1, img2, padding, octaves, want_maps=False)
+
+is the forward-only per-octave stage (2x box-downscaled octaves; per octave the
+luminance term l, the contrast-structure term cs and S = l * cs, their maps and
+per-image means).
 """
 from __future__ import annotations
 
@@ -37,6 +43,8 @@ __all__ = [
     "ssim3d_bwd",
     "ssim_fwd_bwd",
     "ssim3d_fwd_bwd",
+    "ssim_pyramid",
+    "pyramid_extents",
     "workspace_bytes",
     "saved_bytes",
     "window",
@@ -205,6 +213,53 @@ def ssim3d_fwd_bwd(img1, img2, padding, dL, out_mean, grad1, grad2=None, out_map
                             _abi.ptr(grad2), _abi.ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(img1))
     _abi.check("ssim3d_fwd_bwd", st)
+
+
+def pyramid_extents(H: int, W: int, octaves: int) -> list:
+    """(H_o, W_o) of octaves 0 .. octaves-1: each halves the last, rounding up."""
+    out = []
+    for _ in range(octaves):
+        out.append((H, W))
+        H, W = (H + 1) // 2, (W + 1) // 2
+    return out
+
+
+def ssim_pyramid(img1, img2, padding, octaves: int, want_maps: bool = False, out_means=None,
+                 maps=None, workspace=None):
+    """Per-octave SSIM components of NCHW float32 CUDA images.
+
+    Returns (means, maps): means is a (octaves, 3, N) float32 tensor -- per octave
+    the per-image means of l, cs and S -- and maps, with want_maps (or a given
+    flat ``maps`` buffer), a list of per-octave (3, N, C, Ho, Wo) views of the
+    l, cs and S maps; else None."""
+    _check_pair(img1, img2, 2)
+    N, C, H, W = img1.shape
+    pad = _pad(padding)
+    lib = _abi.load()
+    need = int(lib.gbssim_pyramid_workspace_bytes(N, C, H, W, pad, int(octaves)))
+    if need == 0:
+        raise ValueError(f"invalid shape {tuple(img1.shape)} for {octaves} octaves "
+                         f"with padding {padding!r}")
+    if workspace is None:
+        workspace = _workspace(img1.device, need)
+    if out_means is None:
+        out_means = torch.empty((int(octaves), 3, N), dtype=torch.float32, device=img1.device)
+    if maps is None and want_maps:
+        nf = int(lib.gbssim_pyramid_map_floats(N, C, H, W, pad, int(octaves)))
+        maps = torch.empty(nf, dtype=torch.float32, device=img1.device)
+    st = lib.ssim_pyramid(_abi.ptr(img1), _abi.ptr(img2), N, C, H, W, pad, int(octaves),
+                          _abi.ptr(out_means), _abi.ptr(maps), _abi.ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(img1))
+    _abi.check("ssim_pyramid", st)
+    views = None
+    if maps is not None:
+        views, pos = [], 0
+        for h, w in pyramid_extents(H, W, int(octaves)):
+            ho, wo = (h - 10, w - 10) if pad == VALID else (h, w)
+            n = 3 * N * C * ho * wo
+            views.append(maps[pos:pos + n].view(3, N, C, ho, wo))
+            pos += n
+    return out_means, views
 
 
 # ----------------------------------------------------------------- autograd

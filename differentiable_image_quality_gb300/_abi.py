@@ -33,6 +33,9 @@ SIGNATURES = {
     "ssim_fwd_bwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]),
     "ssim3d_fwd_bwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _fp, _fp, _vp, _sz,
                             _vp]),
+    "gbssim_pyramid_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "gbssim_pyramid_map_floats": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "ssim_pyramid": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _vp, _sz, _vp]),
     "gbssim3d_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gbssim3d_saved_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "ssim3d_fwd": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp, _sz, _i, _vp, _sz, _vp]),

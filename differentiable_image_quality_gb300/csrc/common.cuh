@@ -178,6 +178,22 @@ __device__ __forceinline__ float ssim_value(const Moments &m)
     return (A1 * A2) * rcp_approx(B1 * B2);
 }
 
+// The two factors of S: (l, cs) = (A1 / B1, A2 / B2), S = l * cs.
+__device__ __forceinline__ float2 ssim_factors(const Moments &m)
+{
+    const float2 M = make_float2(m.m1, m.m2);
+    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 msq = __fmul2_rn(M, M);
+    const float2 musq = __fmul2_rn(mu, mu);
+    const float ss = m.es - (msq.x + msq.y);
+    const float s12 = fmaf(-m.m1, m.m2, m.e12);
+    const float B1 = (musq.x + musq.y) + kC1;
+    const float B2 = ss + kC2;
+    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
+    const float A2 = fmaf(2.0f, s12, kC2);
+    return __fmul2_rn(make_float2(A1, A2), make_float2(rcp_approx(B1), rcp_approx(B2)));
+}
+
 // S and its derivatives with respect to the shifted moments, written as
 // S = l * cs with l = A1 / B1 (luminance) and cs = A2 / B2 (contrast-structure):
 //   dS/dsigma_sum = -cs * l / B2,   dS/dsigma12 = 2 l / B2,
@@ -271,6 +287,47 @@ __device__ __forceinline__ void finish_means(double *partials, unsigned *counter
             mean[n] = static_cast<float>(t / count);
         }
         __syncthreads();
+    }
+    if (threadIdx.x == 0) *counter = 0u;
+}
+
+// finish_means for K quantities at once: partials holds K arrays of `stride`
+// doubles (this block's sums already written at each), mean holds K arrays of
+// `images` floats.  One completion ticket per block; the last block reduces
+// every quantity of every image in the same fixed order as finish_means.
+template <int NT, int K>
+__device__ __forceinline__ void finish_means_k(double *partials, int stride, unsigned *counter,
+                                               float *mean, int images, int blocks_per_image,
+                                               double count)
+{
+    __shared__ bool last;
+    __shared__ double wsum[NT / 32];
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned ticket = atomicAdd(counter, 1u);
+        last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < images; ++n) {
+            const double *p = partials + size_t(k) * stride + size_t(n) * blocks_per_image;
+            double s = 0.0;
+            for (int b = threadIdx.x; b < blocks_per_image; b += NT) s += __ldcg(p + b);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+            if (lane == 0) wsum[warp] = s;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                double t = 0.0;
+#pragma unroll
+                for (int w = 0; w < NT / 32; ++w) t += wsum[w];
+                mean[k * images + n] = static_cast<float>(t / count);
+            }
+            __syncthreads();
+        }
     }
     if (threadIdx.x == 0) *counter = 0u;
 }

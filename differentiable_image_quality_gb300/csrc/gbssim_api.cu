@@ -24,6 +24,7 @@ struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
+    int occ_comp = 0;          // components mode of the forward
     int occ3d[2] = {0, 0};     // statistics kernel, adjoint kernel
 };
 
@@ -58,6 +59,16 @@ int device_info(DeviceInfo **out)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ2d[i], k, kThreads2d, smem);
             if (e != cudaSuccess) return cuda_fail(e);
             if (d.occ2d[i] < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+        }
+        {
+            const void *k = ssim2d_components_kernel_ptr();
+            const size_t smem = ssim2d_smem_bytes(false, false);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(smem));
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_comp, k, kThreads2d, smem);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (d.occ_comp < 1) return cuda_fail(cudaErrorInvalidConfiguration);
         }
         const cudaError_t e3 = ssim3d_prepare(d.occ3d);
         if (e3 != cudaSuccess) return cuda_fail(e3);
@@ -344,6 +355,53 @@ Layout3d layout3d(int N, int C, int D, int H, int W, int padding)
     return l;
 }
 
+// ---- per-octave maps
+
+constexpr int kMaxOctaves = 32;
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace of ssim_pyramid: the completion counter, 3 x (most blocks of any
+// octave) partial sums, then the downscaled pair of each octave >= 1 (every
+// image 256-byte aligned).
+struct PyrLayout {
+    int octaves = 0;
+    int H[kMaxOctaves], W[kMaxOctaves];
+    size_t x_off[kMaxOctaves], y_off[kMaxOctaves];
+    size_t map_floats = 0, total = 0;
+};
+
+bool pyramid_layout(int N, int C, int H, int W, int padding, int octaves, PyrLayout &L)
+{
+    if (octaves < 1 || octaves > kMaxOctaves || !shape2d_ok(N, C, H, W, padding)) return false;
+    const long long planes = (long long)N * C;
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    long long max_blocks = 0;
+    int h = H, w = W;
+    L.octaves = octaves;
+    L.map_floats = 0;
+    for (int o = 0; o < octaves; ++o) {
+        if (!extent_ok(h, padding) || !extent_ok(w, padding)) return false;
+        L.H[o] = h;
+        L.W[o] = w;
+        const int ho = out_extent(h, padding), wo = out_extent(w, padding);
+        max_blocks = std::max(max_blocks, max_blocks2d(planes, h, w, ho, wo, off));
+        L.map_floats += 3 * size_t(planes) * size_t(ho) * size_t(wo);
+        h = (h + 1) / 2;
+        w = (w + 1) / 2;
+    }
+    size_t pos = round256(kCounterBytes + 3 * size_t(max_blocks) * sizeof(double));
+    L.x_off[0] = L.y_off[0] = 0;
+    for (int o = 1; o < octaves; ++o) {
+        const size_t img = round256(size_t(planes) * L.H[o] * L.W[o] * sizeof(float));
+        L.x_off[o] = pos;
+        L.y_off[o] = pos + img;
+        pos += 2 * img;
+    }
+    L.total = pos;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -529,6 +587,92 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), s));
 }
 
+
+size_t gbssim_pyramid_workspace_bytes(int N, int C, int H, int W, int padding, int octaves)
+{
+    PyrLayout L;
+    return pyramid_layout(N, C, H, W, padding, octaves, L) ? L.total : 0;
+}
+
+size_t gbssim_pyramid_map_floats(int N, int C, int H, int W, int padding, int octaves)
+{
+    PyrLayout L;
+    return pyramid_layout(N, C, H, W, padding, octaves, L) ? L.map_floats : 0;
+}
+
+int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+                 int octaves, float *out_means, float *maps_or_null, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_means)) ||
+        (rc = check_opt(maps_or_null)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    PyrLayout L;
+    if (!pyramid_layout(N, C, H, W, padding, octaves, L)) return GBSSIM_ESHAPE;
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+        workspace_bytes < L.total)
+        return GBSSIM_EWORKSPACE;
+    const long long planes = (long long)N * C;
+    const size_t img_bytes = size_t(planes) * H * W * sizeof(float);
+    const size_t map_bytes = L.map_floats * sizeof(float);
+    const size_t mean_bytes = size_t(octaves) * 3 * N * sizeof(float);
+    if (overlaps(maps_or_null, map_bytes, img1, img_bytes) ||
+        overlaps(maps_or_null, map_bytes, img2, img_bytes) ||
+        overlaps(maps_or_null, map_bytes, out_means, mean_bytes) ||
+        overlaps(out_means, mean_bytes, img1, img_bytes) ||
+        overlaps(out_means, mean_bytes, img2, img_bytes) ||
+        overlaps(workspace, workspace_bytes, img1, img_bytes) ||
+        overlaps(workspace, workspace_bytes, img2, img_bytes))
+        return GBSSIM_EINVAL;
+
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    const float *cx = img1, *cy = img2;
+    size_t map_pos = 0;
+    for (int o = 0; o < octaves; ++o) {
+        const int h = L.H[o], w = L.W[o];
+        if (o > 0) {
+            float *ox = reinterpret_cast<float *>(ws + L.x_off[o]);
+            float *oy = reinterpret_cast<float *>(ws + L.y_off[o]);
+            const cudaError_t e =
+                downscale2x_launch(cx, cy, ox, oy, planes, L.H[o - 1], L.W[o - 1], d->sm_count, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+            cx = ox;
+            cy = oy;
+        }
+        const int ho = out_extent(h, padding), wo = out_extent(w, padding);
+        const Plan2d p = cached_plan2d(planes, h, w, ho, wo, off, false, d->sm_count, d->occ_comp);
+        if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+        Ssim2dArgs a{};
+        a.x = cx; a.y = cy;
+        a.H = h; a.W = w; a.Ho = ho; a.Wo = wo;
+        a.off = off;
+        a.C = C;
+        set_segments(a, p, ho);
+        a.vec16 = (w % 4 == 0) && (reinterpret_cast<uintptr_t>(cx) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(cy) % 16 == 0);
+        ssim2d_prepare_staging(a, planes, false);
+        a.inv_count = float(1.0 / (double(C) * double(ho) * double(wo)));
+        a.map = maps_or_null ? maps_or_null + map_pos : nullptr;
+        a.map_stride = size_t(planes) * ho * wo;
+        a.segments = int(p.blocks);
+        a.counter = reinterpret_cast<unsigned *>(ws);
+        a.partials = reinterpret_cast<double *>(ws + kCounterBytes);
+        a.mean = out_means + size_t(o) * 3 * N;
+        a.images = N;
+        a.blocks_per_image = int(p.blocks / N);
+        a.count = double(C) * double(ho) * double(wo);
+        const cudaError_t e = ssim2d_components_launch(a, int(p.blocks), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        map_pos += 3 * a.map_stride;
+    }
+    return GBSSIM_OK;
+}
 
 size_t gbssim3d_workspace_bytes(int N, int C, int D, int H, int W, int padding)
 {

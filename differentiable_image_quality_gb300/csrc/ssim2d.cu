@@ -30,6 +30,10 @@
 // passes use the window's symmetry (w_k = w_{10-k}): five paired sums, then six
 // multiply-adds, which also halves the length of each dependent chain.
 //
+// Components mode (forward only) writes the two factors of S = l * cs as well:
+// the per-octave stage of a multi-scale comparison consumes l, cs and S maps
+// and their per-image means.
+//
 // Gradient mode has two uses:
 //   training forward: the gradient fields of mean[n] itself (dL = 1) go to the
 //                     caller's `saved` buffer, and the mean is reduced too;
@@ -195,10 +199,11 @@ __device__ __forceinline__ SegWork segment_of(const Ssim2dArgs &a, int b)
 template <bool GRAD, bool G2>
 constexpr int min_blocks() { return (GRAD && G2) ? 2 : 3; }
 
-template <bool GRAD, bool G2>
+template <bool GRAD, bool G2, bool COMP = false>
 __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     ssim2d_stream_kernel(const __grid_constant__ Ssim2dArgs a)
 {
+    static_assert(!(COMP && GRAD), "components mode is forward only");
     constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
     constexpr int NGH = SW / KH;
     static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     float *vc = reinterpret_cast<float *>(gbase + kPairPlane);
     float *cbx = reinterpret_cast<float *>(gbase + kPairPlane + (G2 ? kPairPlane : kOnePlane));
     float *cby = cbx + CBB;
-    __shared__ double red[NT / 32];
+    __shared__ double red[COMP ? 3 : 1][NT / 32];
     __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
     const int tid = threadIdx.x;
@@ -496,6 +501,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     const bool col_own = GRAD ? (tid >= 10 || strip == 0) : true;
     const bool want_mean = (a.partials != nullptr);
     float ssum = 0.0f;
+    float lsum = 0.0f, csum = 0.0f;  // components mode: sums of l and cs
     // Columns the strip needs (the last strip of a plane is usually narrower):
     // statistic columns tid < nstat, gradient columns jj < ngrad.  Row-pass
     // groups and column-pass warps wholly beyond them are skipped; the entries
@@ -575,6 +581,18 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
             va[k * P2 + tid] = ring_sum2<k>(gA);
             if (G2) vb2[k * P2 + tid] = ring_sum2<k>(gB);
             else vc[k * P1 + tid] = ring_sum1<k>(gC);
+        } else if (COMP) {
+            const float2 lc = ssim_factors(mo);
+            const float S = lc.x * lc.y;
+            lsum += ok ? lc.x : 0.0f;
+            csum += ok ? lc.y : 0.0f;
+            ssum += ok ? S : 0.0f;
+            if (a.map && ok) {
+                float *m = a.map + (size_t(plane) * a.Ho + p) * a.Wo + pc;
+                m[0] = lc.x;
+                m[a.map_stride] = lc.y;
+                m[2 * a.map_stride] = S;
+            }
         } else {
             const float S = ssim_value(mo);
             ssum += ok ? S : 0.0f;
@@ -651,9 +669,24 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     }
 
     if (want_mean) {
-        const double tot = block_sum<NT>(ssum, red);
-        if (tid == 0) a.partials[w.slot] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
-        finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
+        const double nan = __longlong_as_double(0x7ff8000000000000LL);
+        if (COMP) {
+            // three sums (l, cs, S); partials and means are [3][...]
+            const double tl = block_sum<NT>(lsum, red[0]);
+            const double tc = block_sum<NT>(csum, red[1]);
+            const double ts = block_sum<NT>(ssum, red[2]);
+            if (tid == 0) {
+                a.partials[w.slot] = failed ? nan : tl;
+                a.partials[a.segments + w.slot] = failed ? nan : tc;
+                a.partials[2 * a.segments + w.slot] = failed ? nan : ts;
+            }
+            finish_means_k<NT, 3>(a.partials, a.segments, a.counter, a.mean, a.images,
+                                  a.blocks_per_image, a.count);
+        } else {
+            const double tot = block_sum<NT>(ssum, red[0]);
+            if (tid == 0) a.partials[w.slot] = failed ? nan : tot;
+            finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
+        }
     }
 }
 
@@ -728,11 +761,41 @@ bool encode_rows_map(CUtensorMap &m, const float *ptr, long long planes, int H, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool GRAD, bool G2>
+template <bool GRAD, bool G2, bool COMP = false>
 cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
 {
-    ssim2d_stream_kernel<GRAD, G2><<<blocks, NT, smem_bytes(GRAD, G2), s>>>(a);
+    ssim2d_stream_kernel<GRAD, G2, COMP><<<blocks, NT, smem_bytes(GRAD, G2), s>>>(a);
     return cudaGetLastError();
+}
+
+// Both images one octave down: out(i, j) = mean of the in-range pixels of the
+// 2x2 block at (2i, 2j); planes of H x W -> Hd x Wd = ceil(H/2) x ceil(W/2).
+__global__ void __launch_bounds__(256) downscale2x_kernel(const float *__restrict__ x,
+                                                          const float *__restrict__ y,
+                                                          float *__restrict__ ox,
+                                                          float *__restrict__ oy, int H, int W,
+                                                          size_t total)
+{
+    const int Hd = (H + 1) >> 1, Wd = (W + 1) >> 1;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += size_t(gridDim.x) * blockDim.x) {
+        const int j = int(i % size_t(Wd));
+        const size_t t = i / size_t(Wd);
+        const int r = int(t % size_t(Hd));
+        const size_t plane = t / size_t(Hd);
+        const int r0 = 2 * r, c0 = 2 * j;
+        const bool r1 = r0 + 1 < H, c1 = c0 + 1 < W;
+        const size_t b = (plane * size_t(H) + r0) * size_t(W) + c0;
+        float sx = x[b], sy = y[b];
+        if (c1) { sx += x[b + 1]; sy += y[b + 1]; }
+        if (r1) {
+            sx += x[b + W]; sy += y[b + W];
+            if (c1) { sx += x[b + W + 1]; sy += y[b + W + 1]; }
+        }
+        const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
+        ox[i] = sx * inv;
+        oy[i] = sy * inv;
+    }
 }
 
 }  // namespace
@@ -780,6 +843,28 @@ const void *ssim2d_kernel_ptr(bool grad, bool g2)
     if (!grad) return reinterpret_cast<const void *>(ssim2d_stream_kernel<false, false>);
     return g2 ? reinterpret_cast<const void *>(ssim2d_stream_kernel<true, true>)
               : reinterpret_cast<const void *>(ssim2d_stream_kernel<true, false>);
+}
+
+cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s)
+{
+    return launch_stream<false, false, true>(a, blocks, s);
+}
+
+const void *ssim2d_components_kernel_ptr()
+{
+    return reinterpret_cast<const void *>(ssim2d_stream_kernel<false, false, true>);
+}
+
+cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
+                               long long planes, int H, int W, int sm_count, cudaStream_t s)
+{
+    const size_t total = size_t(planes) * size_t((H + 1) / 2) * size_t((W + 1) / 2);
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = size_t(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    downscale2x_kernel<<<unsigned(blocks), 256, 0, s>>>(x, y, ox, oy, H, W, total);
+    return cudaGetLastError();
 }
 
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)

@@ -33,6 +33,8 @@ struct Ssim2dArgs {
     const float *dL;  // [N] or null (then dL = 1)
     float inv_count;  // 1 / (C * Ho * Wo)
     float *map;       // [planes, Ho, Wo] or null
+    size_t map_stride;  // components mode: floats from the l map to the cs map (cs to S)
+    int segments;       // blocks of the launch (components mode: partials are [3][segments])
     // mean reduction (null partials: no mean)
     double *partials;
     unsigned *counter;
@@ -56,6 +58,14 @@ void ssim2d_set_staging_mode(int mode);
 int ssim2d_strips(bool grad, int W, int Wo, int off);
 const void *ssim2d_kernel_ptr(bool grad, bool g2);
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s);
+// Forward-only kernel in components mode: l, cs and S maps (a.map, a.map_stride
+// apart) and their per-image means a.mean[j * images + n], j = 0 (l), 1 (cs),
+// 2 (S); a.partials holds 3 x a.segments doubles.  Same plan as the forward.
+cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s);
+const void *ssim2d_components_kernel_ptr();
+// Both images one octave down (2x2 box means, ragged edges over in-range pixels).
+cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
+                               long long planes, int H, int W, int sm_count, cudaStream_t s);
 
 // g = f * dL[i / per_image] * inv_count for one or two fields (f2/g2 may be null).
 cudaError_t scale_fields_launch(const float *f1, const float *f2, float *g1, float *g2,

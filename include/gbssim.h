@@ -157,6 +157,45 @@ int ssim_fwd_noalloc(const float *img1, const float *img2, int N, int C, int H, 
                      int padding, float *out_mean, float *out_map_or_null, float *saved_or_null,
                      size_t saved_bytes, int want_grad2, void *stream);
 
+/* ------------------------------------------------------- per-octave maps --- */
+/* The per-octave stage of the ssimulacra2 hand-off page ("blur -> pointwise
+ * sigma11 / sigma22 / sigma12 -> error maps", once per octave of a 2x pyramid),
+ * with this library's 11x11 Gaussian window in place of that metric's
+ * recursive blur and with SSIM's own three per-pixel maps as the error maps:
+ *   l  = (2 mu1 mu2 + C1) / (mu1^2 + mu2^2 + C1)       luminance
+ *   cs = (2 sigma12 + C2) / (sigma11 + sigma22 + C2)   contrast-structure
+ *   S  = l * cs                                         SSIM (as ssim_fwd)
+ * Octave 0 is the input pair; octave o + 1 is octave o downscaled 2x: each pixel
+ * is the mean of the pixels of its 2x2 block that lie inside the image (so
+ * ceil(H/2) x ceil(W/2); a ragged last row or column averages one or two
+ * pixels).  The page gives no formula for the downscale or the error maps;
+ * these are the plain readings.  Forward only; no gradients. */
+
+/* Extents (H_o, W_o) of octave o: H_0 = H, H_{o+1} = ceil(H_o / 2). */
+
+/* Workspace bytes of ssim_pyramid (0 if a shape or octave count is invalid:
+ * octaves >= 1 and every octave extent must suit the padding, i.e. >= 11 for
+ * valid).  Same zero-fill rule as gbssim_workspace_bytes.  It holds the
+ * downscaled images of octaves 1 .. octaves-1 and the block partial sums. */
+size_t gbssim_pyramid_workspace_bytes(int N, int C, int H, int W, int padding, int octaves);
+
+/* Floats of the optional maps buffer: per octave o, three maps of
+ * N*C*Ho_o*Wo_o floats (l, then cs, then S), octaves one after another.  0 if
+ * invalid. */
+size_t gbssim_pyramid_map_floats(int N, int C, int H, int W, int padding, int octaves);
+
+/* Per-octave means and maps.
+ *   img1, img2    [N, C, H, W] float32, device.
+ *   octaves       number of octaves (>= 1).
+ *   out_means     [octaves][3][N] float32, device: per octave the mean of l, of
+ *                 cs and of S over the channels and output pixels of image n.
+ *   maps_or_null  device buffer of gbssim_pyramid_map_floats(...) floats, or NULL.
+ *   workspace     device buffer of gbssim_pyramid_workspace_bytes(...) bytes.
+ * Octave 0's S mean equals ssim_fwd's mean. */
+int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int W, int padding,
+                 int octaves, float *out_means, float *maps_or_null, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------------------ 3D ----- */
 /* fused-ssim README, "3D data": the same statistics with an 11x11x11 window on
  * NCDHW volumes.  Arguments mean what they mean in 2D, with D added; both

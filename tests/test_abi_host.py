@@ -155,3 +155,31 @@ def test_3d_argument_errors(lib):
     assert bwd(wsb=ws - 1) == EWORKSPACE
     assert bwd(g1=(1 << 30) + 4) == EINVAL
     assert bwd(saved=4 << 30, sb=n - 4, wsp=None) == EWORKSPACE
+
+
+def test_pyramid_sizes_and_argument_errors(lib):
+    # 64 x 64 valid: octave extents 64, 32, 16 (outputs 54, 22, 6); a fourth (8) is too small
+    per = [54 * 54, 22 * 22, 6 * 6]
+    assert lib.gbssim_pyramid_map_floats(1, 3, 64, 64, 0, 3) == 3 * 3 * sum(per)
+    assert lib.gbssim_pyramid_map_floats(1, 3, 64, 64, 0, 4) == 0
+    assert lib.gbssim_pyramid_workspace_bytes(1, 3, 64, 64, 0, 4) == 0
+    assert lib.gbssim_pyramid_workspace_bytes(1, 3, 64, 64, 0, 0) == 0
+    assert lib.gbssim_pyramid_workspace_bytes(1, 3, 64, 64, 1, 7) > 0  # same: down to 1 x 1
+    ws = lib.gbssim_pyramid_workspace_bytes(1, 3, 64, 64, 0, 3)
+    # the downscaled pairs of octaves 1 and 2 live in the workspace
+    assert ws >= 2 * 3 * (32 * 32 + 16 * 16) * 4
+
+    def pyr(img1=1 << 30, img2=2 << 30, octaves=3, pad=0, means=3 << 30, maps=None,
+            wsp=FAKE * 256, wsb=ws):
+        return lib.ssim_pyramid(img1, img2, 1, 3, 64, 64, pad, octaves, means, maps, wsp, wsb,
+                                None)
+
+    assert pyr(img1=None) == EINVAL
+    assert pyr(means=None) == EINVAL
+    assert pyr(means=(3 << 30) + 2) == EALIGN
+    assert pyr(pad=4) == EINVAL
+    assert pyr(octaves=4) == ESHAPE
+    assert pyr(octaves=0) == ESHAPE
+    assert pyr(wsb=ws - 1) == EWORKSPACE
+    assert pyr(wsp=FAKE * 256 + 16) == EWORKSPACE
+    assert pyr(maps=(1 << 30) + 64) == EINVAL  # maps overlapping img1
