@@ -134,6 +134,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, i
         : "memory");
 }
 
+// The same for a 4D box at (x, y, z, w).
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *map, int x, int y, int z, int w,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Approximate reciprocal (the hardware instruction, relative error ~1 ulp).
 // Its argument here is a product of two sums each >= C1 or C2, never zero,
 // infinite or subnormal.

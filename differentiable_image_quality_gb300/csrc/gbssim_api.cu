@@ -446,7 +446,12 @@ int gbssim_device_status(unsigned *flags_out)
 {
     if (!flags_out) return GBSSIM_EINVAL;
     *flags_out = 0;
-    return cuda_fail(ssim2d_staging_status(flags_out, true));
+    unsigned f3 = 0;
+    const cudaError_t e = ssim2d_staging_status(flags_out, true);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const cudaError_t e3 = ssim3d_staging_status(&f3, true);
+    *flags_out |= f3;
+    return cuda_fail(e3);
 }
 
 size_t gbssim_workspace_bytes(int N, int C, int H, int W, int padding)
@@ -706,6 +711,7 @@ static void fill3d(Ssim3dArgs &a, const float *x, const float *y, int N, int C, 
     a.inv_count = float(1.0 / (double(C) * a.Do * a.Ho * a.Wo));
     a.count = double(C) * a.Do * a.Ho * a.Wo;
     a.images = N;
+    ssim3d_prepare_staging(a, (long long)N * C);
 }
 
 static void apply_plan(Ssim3dArgs &a, const Plan3d &p)

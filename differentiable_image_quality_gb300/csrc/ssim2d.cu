@@ -821,6 +821,26 @@ void ssim2d_prepare_staging(Ssim2dArgs &a, long long planes, bool grad)
 
 void ssim2d_set_staging_mode(int mode) { g_staging_mode = (mode >= 0 && mode <= 2) ? mode : 0; }
 
+int staging_mode() { return g_staging_mode; }
+
+bool encode_tiled_f32(CUtensorMap &m, const void *ptr, int rank, const unsigned long long *dims,
+                      const unsigned long long *strides, const unsigned *box)
+{
+    const auto enc = tensor_map_encoder();
+    if (!enc || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<void *>(ptr), d,
+               st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t ssim2d_staging_status(unsigned *flags, bool clear)
 {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_staging_status, sizeof(unsigned));

@@ -54,6 +54,11 @@ cudaError_t ssim2d_staging_status(unsigned *flags, bool clear);
 // that announce 16 bytes more than they deliver, so that every wait runs out
 // (test of the failure path).
 void ssim2d_set_staging_mode(int mode);
+int staging_mode();  // the mode set last (also applied to the 3D kernels)
+// A tiled float32 tensor map: rank dims (innermost first), rank - 1 byte strides,
+// box extents; out-of-range elements read as zeros.  False if encoding fails.
+bool encode_tiled_f32(CUtensorMap &m, const void *ptr, int rank, const unsigned long long *dims,
+                      const unsigned long long *strides, const unsigned *box);
 // Column strips of a plane in gradient mode (over W) or forward-only mode (over Wo).
 int ssim2d_strips(bool grad, int W, int Wo, int off);
 const void *ssim2d_kernel_ptr(bool grad, bool g2);

@@ -4,8 +4,12 @@
 // Following that page's plan -- keep the 2D convolution on XY slices, and do
 // the Z convolution and SSIM through a ring buffer, one depth row per thread --
 // a CTA owns an XY tile of 16 x 16 columns and walks along Z one slice per step:
-//   XY  the slice's row pass and column pass in shared memory (cp.async staging
-//       of the slice tile plus its 10-pixel halo, three buffers);
+//   XY  the slice's row pass and column pass in shared memory (the slice tile
+//       plus its 10-pixel halo staged by tensor copies -- one thread issues
+//       them, a transaction barrier per buffer tracks them, every wait bounded
+//       -- or by cp.async where the tile does not start on a 16-byte column;
+//       NBUF buffers, a slice's copies issued NBUF - 3 steps before it is
+//       waited for);
 //   Z   each thread keeps an 11-slice register ring of its column's XY-blurred
 //       values; the ring's weighted sum is the full 3D window.
 // Two kernels:
@@ -21,6 +25,7 @@
 // the row passes are numbered row-fastest over odd shared-memory pitches, so
 // the threads of a quarter warp hit distinct bank groups.
 #include "common.cuh"
+#include "ssim2d.cuh"
 #include "ssim3d.cuh"
 
 namespace gbssim {
@@ -35,16 +40,29 @@ constexpr int GXP = IX + 1;      // float4 pitch of a staged derivative row (27)
 constexpr int HXP = TX + 1;      // float4 pitch of a row-pass output row (17)
 constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;   // row-pass items per slice (104)
 constexpr int KY = 2, NYG = TY / KY, NYI = NYG * TX;   // column-pass items per slice (128)
-constexpr int NBUF = 3;
+constexpr int NBUF = 6;      // staged slices in flight
+constexpr int CBUF = NBUF + 1;  // adjoint: chain-rule pixel tiles in flight
 
 static_assert(NT == TY * TX, "one thread per column of the tile");
 static_assert(NYI % 32 == 0, "column-pass items fill whole warps");
 static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
 
-constexpr size_t kStatsInBytes = size_t(2) * NBUF * IY * IXP * sizeof(float);
-constexpr size_t kAdjInBytes = size_t(NBUF) * IY * GXP * sizeof(float4);
+// Staging buffers, each a multiple of 128 bytes (tensor-copy destinations).
+constexpr int XSTAGE = (IY * IXP + 31) / 32 * 32;  // floats of a staged input tile
+constexpr int GSTAGE = (IY * GXP + 7) / 8 * 8;     // float4 of a staged derivative tile
+constexpr int CSTAGE = TY * TX;                     // floats of a chain-rule pixel tile
+constexpr unsigned kStatsTx = 2u * IY * IXP * sizeof(float);
+constexpr unsigned kAdjTx = unsigned(IY * GXP * sizeof(float4) + 2 * CSTAGE * sizeof(float));
+constexpr long long kWaitCycles = 1LL << 31;   // staging wait limit (about a second)
+constexpr long long kDrainCycles = 1LL << 27;  // after a failed wait: copies still in flight
+
+__device__ unsigned g_staging3d_status;  // bit 0: a staging wait ran out of time
+
+constexpr size_t kStatsInBytes = size_t(2) * NBUF * XSTAGE * sizeof(float);
+constexpr size_t kAdjInBytes = size_t(NBUF) * GSTAGE * sizeof(float4);
+constexpr size_t kChainBytes = size_t(2) * CBUF * CSTAGE * sizeof(float);
 constexpr size_t kXBytes = size_t(2) * IY * HXP * sizeof(float4);
-constexpr size_t kYBytes = size_t(TY) * TX * sizeof(float4);
+constexpr size_t kYBytes = size_t(2) * TY * TX * sizeof(float4);  // two slices
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
@@ -93,15 +111,29 @@ __device__ __forceinline__ void taps4(const float4 *src, int stride, float2 (&oa
 
 // ------------------------------------------------------------------ kernel A
 
-template <bool GRAD>
-__global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
+// Slices j < waited have been waited for, j < issued copied: after a failed
+// wait, let the copies still in flight land (bounded), then record the failure.
+__device__ __forceinline__ void drain_failed(uint64_t *bars, int waited, int issued)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const long long t0 = clock64();
+    for (int j = waited; j < issued; ++j) {
+        const long long left = kDrainCycles - (clock64() - t0);
+        if (left > 0) mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, left);
+    }
+    atomicOr(&g_staging3d_status, 1u);
+}
+
+template <bool GRAD>
+__global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const __grid_constant__ Ssim3dArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem_dyn[];
+    unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
     float *xs = reinterpret_cast<float *>(smem_raw);
-    float *ys = xs + NBUF * IY * IXP;
+    float *ys = xs + NBUF * XSTAGE;
     float4 *hx = reinterpret_cast<float4 *>(smem_raw + kStatsInBytes);
     float4 *hy = hx + 2 * IY * HXP;
     __shared__ double red[NT / 32];
+    __shared__ uint64_t bars[NBUF];
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -122,6 +154,14 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
     auto load_slice = [&](int s) {
         const int buf = s % NBUF;
         const int Z = iz0 + s;
+        if (a.tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars[buf], kStatsTx + a.tx_extra);
+                tma_load_4d(xs + buf * XSTAGE, &a.tm_x, ix0, iy0, Z, plane, &bars[buf]);
+                tma_load_4d(ys + buf * XSTAGE, &a.tm_y, ix0, iy0, Z, plane, &bars[buf]);
+            }
+            return;
+        }
         const bool zin = (Z >= 0) && (Z < a.D);
         if (a.vec16) {
             // the tile origin ix0 is a multiple of 4 and W % 4 == 0: 16-byte chunks,
@@ -132,7 +172,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
                 const int Y = iy0 + r, X = ix0 + 4 * ch;
                 const bool inb = zin && (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
                 const size_t gi = inb ? (size_t(Z) * a.H + Y) * a.W + X : 0;
-                const int si = (buf * IY + r) * IXP + 4 * ch;
+                const int si = buf * XSTAGE + r * IXP + 4 * ch;
                 cp_async16(xs + si, xp + gi, inb);
                 cp_async16(ys + si, yp + gi, inb);
             }
@@ -143,7 +183,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
             const int Y = iy0 + r, X = ix0 + c;
             const bool inb = zin && (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
             const size_t gi = inb ? (size_t(Z) * a.H + Y) * a.W + X : 0;
-            const int si = (buf * IY + r) * IXP + c;
+            const int si = buf * XSTAGE + r * IXP + c;
             cp_async4(xs + si, xp + gi, inb);
             cp_async4(ys + si, yp + gi, inb);
         }
@@ -152,7 +192,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
     // row pass of slice s: staged row r, columns [KX g, KX g + KX)
     auto x_item = [&](int s, int item) {
         const int g = item / IY, r = item - g * IY;
-        const int base = ((s % NBUF) * IY + r) * IXP + g * KX;
+        const int base = (s % NBUF) * XSTAGE + r * IXP + g * KX;
         float xv[KX + 10], yv[KX + 10];
 #pragma unroll
         for (int m = 0; m < KX + 8; m += 4) {
@@ -195,7 +235,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
         taps4<KY>(hx + ((s & 1) * IY + g * KY) * HXP + tx, HXP, oa, ob);
 #pragma unroll
         for (int o = 0; o < KY; ++o)
-            hy[(g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
+            hy[((s & 1) * TY + g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
     };
 
     const int ty = tid / TX, tx = tid - ty * TX;
@@ -209,7 +249,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
     // Z step: push this column's XY-blurred value of slice s, finish slice s - 10.
     auto z_step = [&](auto K_, int s) {
         constexpr int K = decltype(K_)::value;
-        const float4 h = hy[ty * TX + tx];
+        const float4 h = hy[((s & 1) * TY + ty) * TX + tx];
         rA[K] = lo(h);
         rB[K] = hi(h);
         const int p = z0 + s - 10;
@@ -231,38 +271,81 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
     };
 #define GBSSIM_ZA(K) z_step(std::integral_constant<int, K>{}, s)
 
-    load_slice(0);
-    cp_async_commit();
-    if (nz > 1) load_slice(1);
-    cp_async_commit();
-    if (nz > 2) load_slice(2);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    for (int i = tid; i < NXI; i += NT) x_item(0, i);
-    __syncthreads();
-
-    for (int s = 0; s < nz; ++s) {
-        const int nx = (s + 1 < nz) ? NXI : 0;
-        for (int i = tid; i < NYI + nx; i += NT) {
-            if (i < NYI)
-                y_item(s, i);
-            else
-                x_item(s + 1, i - NYI);
+    // Pipeline: step s runs the Z pass of slice s, the column pass of slice
+    // s + 1 and the row pass of slice s + 2, then one barrier.  The row and
+    // column results are double-buffered by slice parity, so each buffer a step
+    // writes was last read in the step before.  Slices 0 .. NBUF-1 are in flight
+    // from the start (one commit group each); slice s + NBUF is issued at step s
+    // into the buffer the row pass of slice s released two steps earlier.
+    // Tensor staging waits on slice j's barrier (use j / NBUF of buffer
+    // j % NBUF); a wait that runs out stops the walk (the block's mean is NaN).
+    auto landed = [&](int j) {
+        return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
+    };
+    if (a.tma) {
+        if (tid == 0) {
+#pragma unroll
+            for (int b = 0; b < NBUF; ++b) mbar_init(&bars[b], 1);
+            mbar_init_fence();
         }
         __syncthreads();
-        if (s + 3 < nz) load_slice(s + 3);  // into the buffer x_item(s) released
+    }
+    int issued = 0, waited = 0;  // slices copied / waited for (uniform)
+#pragma unroll
+    for (int k = 0; k < NBUF; ++k) {
+        if (k < nz) {
+            load_slice(k);
+            ++issued;
+        }
         cp_async_commit();
-        GBSSIM_RING_SWITCH(s, GBSSIM_ZA)
-        cp_async_wait<1>();  // slice s + 2 has landed
+    }
+    bool ok = true;
+    if (a.tma) ok = landed(0) && landed(1);
+    else cp_async_wait<NBUF - 2>();  // slices 0 and 1
+    bool failed = __syncthreads_or(!ok);
+    if (!failed) {
+        waited = min(nz, 2);
+        for (int i = tid; i < NXI; i += NT) x_item(0, i);
         __syncthreads();
+        const int nx = (1 < nz) ? NXI : 0;
+        for (int i = tid; i < NYI + nx; i += NT) {
+            if (i < NYI) y_item(0, i);
+            else x_item(1, i - NYI);
+        }
+        if (a.tma) ok = landed(2);
+        else cp_async_wait<NBUF - 3>();  // slice 2
+        failed = __syncthreads_or(!ok);
+        if (!failed) waited = min(nz, 3);
+    }
+
+    for (int s = 0; s < nz && !failed; ++s) {
+        GBSSIM_RING_SWITCH(s, GBSSIM_ZA)
+        const int ny = (s + 1 < nz) ? NYI : 0;
+        const int nx = (s + 2 < nz) ? NXI : 0;
+        for (int i = tid; i < ny + nx; i += NT) {
+            if (i < ny) y_item(s + 1, i);
+            else x_item(s + 2, i - ny);
+        }
+        if (s + NBUF < nz) {
+            load_slice(s + NBUF);
+            ++issued;
+        }
+        cp_async_commit();
+        if (a.tma) ok = landed(s + 3);
+        else cp_async_wait<NBUF - 3>();  // slice s + 3 has landed
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        waited = min(nz, s + 4);
     }
 #undef GBSSIM_ZA
     cp_async_wait<0>();
+    if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
 
     if (a.partials) {
         const double tot = block_sum<NT>(ssum, red);
-        if (tid == 0) a.partials[blockIdx.x] = tot;
+        if (tid == 0) a.partials[blockIdx.x] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
         finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
     }
 }
@@ -270,12 +353,16 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const Ssim3dArgs a)
 // ------------------------------------------------------------------ kernel B
 
 template <bool G2>
-__global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs a)
+__global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][IY][GXP]
-    float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes);     // [2][IY][HXP]
-    float4 *uy = ux + 2 * IY * HXP;                                       // [TY][TX]
+    extern __shared__ __align__(128) unsigned char smem_dyn[];
+    unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
+    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][GSTAGE]
+    float *cbx = reinterpret_cast<float *>(smem_raw + kAdjInBytes);      // [CBUF][TY][TX]
+    float *cby = cbx + CBUF * CSTAGE;
+    float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes + kChainBytes);  // [2][IY][HXP]
+    float4 *uy = ux + 2 * IY * HXP;                                       // [2][TY][TX]
+    __shared__ uint64_t bars[NBUF];
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -297,24 +384,44 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs 
     const int nz = q1 - q0 + 10;
     const float scale = a.dL ? a.dL[n] * a.inv_count : a.inv_count;
 
+    // derivative slice gz0 + s, and the input pixels of gradient slice
+    // q0 + s - 10 (the chain rule of step s) into chain buffer s % CBUF
     auto load_slice = [&](int s) {
         const int buf = s % NBUF;
         const int P = gz0 + s;
+        const int q = q0 + s - 10;
+        if (a.tma) {
+            // zeros outside the derivative domain and the volume; the chain tile
+            // of a warm-up step (q < q0) is loaded but not used
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars[buf], kAdjTx + a.tx_extra);
+                tma_load_4d(gs + buf * GSTAGE, &a.tm_g, 4 * gx0, gy0, P, plane, &bars[buf]);
+                tma_load_4d(cbx + (s % CBUF) * CSTAGE, &a.tm_cx, x0, y0, q, plane, &bars[buf]);
+                tma_load_4d(cby + (s % CBUF) * CSTAGE, &a.tm_cy, x0, y0, q, plane, &bars[buf]);
+            }
+            return;
+        }
         const bool zin = (P >= 0) && (P < a.Do);
         for (int e = tid; e < IY * IX; e += NT) {
             const int r = e / IX, c = e - r * IX;
             const int Y = gy0 + r, X = gx0 + c;
             const bool inb = zin && (Y >= 0) && (Y < a.Ho) && (X >= 0) && (X < a.Wo);
             const size_t gi = inb ? (size_t(P) * a.Ho + Y) * a.Wo + X : 0;
-            cp_async16(gs + (buf * IY + r) * GXP + c, gf + gi, inb);
+            cp_async16(gs + buf * GSTAGE + r * GXP + c, gf + gi, inb);
         }
+        const int ty = tid / TX, tx = tid - ty * TX;  // one pixel per thread (NT == TY * TX)
+        const int qy = y0 + ty, qx = x0 + tx;
+        const bool inb = (q >= q0) && (q < q1) && (qy < a.H) && (qx < a.W);
+        const size_t gi = inb ? plane_off + (size_t(q) * a.H + qy) * a.W + qx : 0;
+        cp_async4(cbx + (s % CBUF) * CSTAGE + tid, a.x + gi, inb);
+        cp_async4(cby + (s % CBUF) * CSTAGE + tid, a.y + gi, inb);
     };
 
     // adjoint row pass: gradient columns [KX g, KX g + KX) of staged row r
     auto x_item = [&](int s, int item) {
         const int g = item / IY, r = item - g * IY;
         float2 oa[KX], ob[KX];
-        taps4<KX>(gs + ((s % NBUF) * IY + r) * GXP + g * KX, 1, oa, ob);
+        taps4<KX>(gs + (s % NBUF) * GSTAGE + r * GXP + g * KX, 1, oa, ob);
         float4 *dst = ux + ((s & 1) * IY + r) * HXP + g * KX;
 #pragma unroll
         for (int o = 0; o < KX; ++o) dst[o] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
@@ -326,7 +433,7 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs 
         taps4<KY>(ux + ((s & 1) * IY + g * KY) * HXP + tx, HXP, oa, ob);
 #pragma unroll
         for (int o = 0; o < KY; ++o)
-            uy[(g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
+            uy[((s & 1) * TY + g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
     };
 
     const int ty = tid / TX, tx = tid - ty * TX;
@@ -336,28 +443,16 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs 
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) rA[k] = rB[k] = f2(0.f, 0.f);
 
-    // the input pixels of the chain rule, fetched one Z step ahead
-    float xn = 0.f, yn = 0.f;
-    auto fetch = [&](int s) {  // pixels of gradient slice q0 + s - 10
-        const int q = q0 + s - 10;
-        if (col_ok && q >= q0 && q < q1) {
-            const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
-            xn = __ldg(a.x + gi);
-            yn = __ldg(a.y + gi);
-        }
-    };
-
     auto z_step = [&](auto K_, int s) {
         constexpr int K = decltype(K_)::value;
-        const float4 h = uy[ty * TX + tx];
+        const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
         rA[K] = lo(h);
         rB[K] = hi(h);
-        const float xc = xn, yc = yn;  // fetched during the previous step
-        fetch(s + 1);
         const int q = q0 + s - 10;
         if (s >= 10 && q < q1 && col_ok) {
             const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
-            const float x = xc - kShift, y = yc - kShift;
+            const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
+            const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
             const float2 vA = ring_sum2<K>(rA);  // (B^T g_m1, B^T g_e)
             const float2 vB = ring_sum2<K>(rB);  // (B^T g_e12, B^T g_m2)
             a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
@@ -366,35 +461,72 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const Ssim3dArgs 
     };
 #define GBSSIM_ZB(K) z_step(std::integral_constant<int, K>{}, s)
 
-    load_slice(0);
-    cp_async_commit();
-    if (nz > 1) load_slice(1);
-    cp_async_commit();
-    if (nz > 2) load_slice(2);
-    cp_async_commit();
-    fetch(0);
-    cp_async_wait<1>();
-    __syncthreads();
-    for (int i = tid; i < NXI; i += NT) x_item(0, i);
-    __syncthreads();
-
-    for (int s = 0; s < nz; ++s) {
-        const int nx = (s + 1 < nz) ? NXI : 0;
-        for (int i = tid; i < NYI + nx; i += NT) {
-            if (i < NYI)
-                y_item(s, i);
-            else
-                x_item(s + 1, i - NYI);
+    // The pipeline of the statistics kernel.  Chain buffer (s + NBUF) % CBUF,
+    // filled at step s, held slice s - 1's pixels, read by the Z pass of the
+    // step before.
+    auto landed = [&](int j) {
+        return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
+    };
+    if (a.tma) {
+        if (tid == 0) {
+#pragma unroll
+            for (int b2 = 0; b2 < NBUF; ++b2) mbar_init(&bars[b2], 1);
+            mbar_init_fence();
         }
         __syncthreads();
-        if (s + 3 < nz) load_slice(s + 3);
+    }
+    int issued = 0, waited = 0;
+#pragma unroll
+    for (int k = 0; k < NBUF; ++k) {
+        if (k < nz) {
+            load_slice(k);
+            ++issued;
+        }
         cp_async_commit();
-        GBSSIM_RING_SWITCH(s, GBSSIM_ZB)
-        cp_async_wait<1>();
+    }
+    bool ok = true;
+    if (a.tma) ok = landed(0) && landed(1);
+    else cp_async_wait<NBUF - 2>();  // slices 0 and 1
+    bool failed = __syncthreads_or(!ok);
+    if (!failed) {
+        waited = min(nz, 2);
+        for (int i = tid; i < NXI; i += NT) x_item(0, i);
         __syncthreads();
+        const int nx = (1 < nz) ? NXI : 0;
+        for (int i = tid; i < NYI + nx; i += NT) {
+            if (i < NYI) y_item(0, i);
+            else x_item(1, i - NYI);
+        }
+        if (a.tma) ok = landed(2);
+        else cp_async_wait<NBUF - 3>();  // slice 2
+        failed = __syncthreads_or(!ok);
+        if (!failed) waited = min(nz, 3);
+    }
+
+    for (int s = 0; s < nz && !failed; ++s) {
+        GBSSIM_RING_SWITCH(s, GBSSIM_ZB)
+        const int ny = (s + 1 < nz) ? NYI : 0;
+        const int nx = (s + 2 < nz) ? NXI : 0;
+        for (int i = tid; i < ny + nx; i += NT) {
+            if (i < ny) y_item(s + 1, i);
+            else x_item(s + 2, i - ny);
+        }
+        if (s + NBUF < nz) {
+            load_slice(s + NBUF);
+            ++issued;
+        }
+        cp_async_commit();
+        if (a.tma) ok = landed(s + 3);
+        else cp_async_wait<NBUF - 3>();  // slice s + 3 (and its chain tile) landed
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        waited = min(nz, s + 4);
     }
 #undef GBSSIM_ZB
     cp_async_wait<0>();
+    if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
 }
 
 template <typename K>
@@ -408,8 +540,45 @@ cudaError_t prepare(K kernel, size_t smem, int *occ)
 
 }  // namespace
 
-size_t ssim3d_stats_smem() { return kStatsInBytes + kXBytes + kYBytes; }
-size_t ssim3d_adjoint_smem() { return kAdjInBytes + kXBytes + kYBytes; }
+size_t ssim3d_stats_smem() { return 128 + kStatsInBytes + kXBytes + kYBytes; }
+size_t ssim3d_adjoint_smem() { return 128 + kAdjInBytes + kChainBytes + kXBytes + kYBytes; }
+
+void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes)
+{
+    const int mode = staging_mode();
+    // vec16: valid padding (tile columns start on 16-byte boundaries),
+    // W % 4 == 0 and 16-byte aligned volumes
+    bool ok = mode != 1 && a.vec16 && a.off == 0 && planes < (1LL << 31);
+    if (ok) {
+        const unsigned long long W = a.W, H = a.H, D = a.D, P = planes;
+        const unsigned long long dims[4] = {W, H, D, P};
+        const unsigned long long st[3] = {W * 4, H * W * 4, D * H * W * 4};
+        const unsigned bx[4] = {IXP, IY, 1, 1}, bc[4] = {TX, TY, 1, 1};
+        ok = encode_tiled_f32(a.tm_x, a.x, 4, dims, st, bx) &&
+             encode_tiled_f32(a.tm_y, a.y, 4, dims, st, bx) &&
+             encode_tiled_f32(a.tm_cx, a.x, 4, dims, st, bc) &&
+             encode_tiled_f32(a.tm_cy, a.y, 4, dims, st, bc);
+    }
+    if (ok) {
+        const unsigned long long Wo = a.Wo, Ho = a.Ho, Do = a.Do, P = planes;
+        const unsigned long long dims[4] = {4 * Wo, Ho, Do, P};
+        const unsigned long long st[3] = {Wo * 16, Ho * Wo * 16, Do * Ho * Wo * 16};
+        const unsigned bg[4] = {4 * GXP, IY, 1, 1};
+        ok = a.gfield && encode_tiled_f32(a.tm_g, a.gfield, 4, dims, st, bg);
+    }
+    a.tma = ok ? 1 : 0;
+    a.tx_extra = (ok && mode == 2) ? 16u : 0u;
+}
+
+cudaError_t ssim3d_staging_status(unsigned *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_staging3d_status, sizeof(unsigned));
+    if (e == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_staging3d_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
 
 cudaError_t ssim3d_prepare(int occ[2])
 {

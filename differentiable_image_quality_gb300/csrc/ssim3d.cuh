@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gbssim {
@@ -15,6 +16,13 @@ constexpr int kTile3dX = 16;
 // kernel tiles the output domain (Do x Ho x Wo); the adjoint kernel tiles the
 // volume (D x H x W).
 struct Ssim3dArgs {
+    // tensor staging (tma = 1): x, y as [planes][D][H][W] with the box of a
+    // staged slice tile (statistics) and of a chain-rule pixel tile (adjoint);
+    // the derivative field as [planes][Do][Ho][4 Wo] floats with the box of a
+    // staged derivative tile.  Passed as a grid constant: read in place.
+    CUtensorMap tm_x, tm_y, tm_g, tm_cx, tm_cy;
+    int tma;
+    unsigned tx_extra;         // test hook: bytes announced beyond the copies (0)
     const float *x, *y;        // img1, img2 [planes, D, H, W]
     int D, H, W;
     int Do, Ho, Wo;
@@ -35,6 +43,13 @@ struct Ssim3dArgs {
 };
 
 size_t ssim3d_stats_smem();
+// Tensor maps of a's staging (a.x, a.y, a.gfield and the extents set); sets
+// a.tma = 1 when every map was encoded and the tiles start on 16-byte columns
+// (valid padding, W % 4 == 0, 16-byte aligned volumes), else 0 (cp.async).
+void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes);
+// Reads (and with clear, resets) the 3D kernels' record of staging waits that
+// ran out of time (bit 0).  Synchronous.
+cudaError_t ssim3d_staging_status(unsigned *flags, bool clear);
 size_t ssim3d_adjoint_smem();
 // Per-device set-up (shared-memory limits); occ[0] / occ[1] = resident CTAs per
 // SM of the statistics / adjoint kernels.

@@ -1,9 +1,10 @@
-"""The two ways the 2D kernels stage input rows, and the bounded staging wait.
+"""The two ways the 2D and 3D kernels stage their inputs, and the bounded
+staging wait.
 
-On 16-byte aligned images with W % 4 == 0 the kernels stage rows with tensor
-copies (one thread per block issues them; a transaction barrier tracks them);
-otherwise, or when the staging hook asks for it, every thread issues cp.async
-copies.  Both must give the oracle's results.  A wait for a tensor copy is
+On 16-byte aligned images with W % 4 == 0 (3D: and valid padding) the
+kernels stage rows and slice tiles with tensor copies (one thread per block
+issues them; a transaction barrier tracks them); otherwise, or when the
+staging hook asks for it, every thread issues cp.async copies.  Both must give the oracle's results.  A wait for a tensor copy is
 bounded: when it runs out, the kernel's blocks stop, the device records the
 failure, the affected means come out NaN, and the context stays usable.  The
 hook's mode 2 makes every wait run out by announcing 16 bytes more than the
@@ -93,4 +94,42 @@ def test_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
     got = _run(dev, x, y, dl, "valid", False, "saved")
     ref = _oracle(oracle_mod, x, y, dl, "valid", False)
     _assert_parity(got, ref, False, "after a staging timeout")
+    assert _status(lib) == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape", [(1, 1, 13, 20, 36), (2, 1, 12, 12, 12)])
+def test_both_3d_staging_paths_match_the_oracle(lib, oracle_mod, shape, mode):
+    import torch
+
+    x, y = uniform_pair(shape, 970 + shape[4], std=0.08)
+    dl = np.linspace(-1.0, 0.5, shape[0])
+    ref = _oracle(oracle_mod, x, y, dl, "valid", True, want_map=True)
+    lib.gbssim_tune_staging(mode)
+    try:
+        for path in ("saved", "recompute"):
+            got = _run(torch.device("cuda:0"), x, y, dl, "valid", True, path, want_map=True)
+            _assert_parity(got, ref, True, f"3D mode {mode} {shape} {path}")
+    finally:
+        lib.gbssim_tune_staging(0)
+
+
+def test_3d_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
+    import torch
+
+    dev = torch.device("cuda:0")
+    assert _status(lib) == 0, "an earlier call recorded a staging timeout"
+    x, y = uniform_pair((1, 1, 14, 16, 16), 991, std=0.08)
+    dl = np.array([-1.0])
+    lib.gbssim_tune_staging(2)
+    try:
+        stalled = _run(dev, x, y, dl, "valid", False, "saved")
+    finally:
+        lib.gbssim_tune_staging(0)
+    assert _status(lib) & STAGING_TIMEOUT
+    assert np.all(np.isnan(stalled["mean"]))
+    assert _status(lib) == 0
+    got = _run(dev, x, y, dl, "valid", False, "saved")
+    ref = _oracle(oracle_mod, x, y, dl, "valid", False)
+    _assert_parity(got, ref, False, "3D after a staging timeout")
     assert _status(lib) == 0
