@@ -306,15 +306,17 @@ struct Plan3d {
     long long blocks = 0;
 };
 
-// Tiles of 16 x 16 columns over (rows, cols), z segments over zlen, with the
-// same per-SM cost model as in 2D (a 10-slice warm-up per segment).
-Plan3d plan3d(long long planes, int zlen, int rows, int cols, int sm_count, int occ)
+// Tiles of 16 x tile_x columns over (rows, cols), z segments over zlen, with the
+// same per-SM cost model as in 2D (a 10-slice warm-up per segment); an SM is
+// taken as saturated at 16 resident warps.
+Plan3d plan3d(long long planes, int zlen, int rows, int cols, int tile_x, int sm_count, int occ)
 {
     Plan3d p;
-    p.tiles_x = int(ceil_div(cols, kTile3dX));
+    p.tiles_x = int(ceil_div(cols, tile_x));
     p.tiles_y = int(ceil_div(rows, kTile3dY));
     const long long per_z = planes * p.tiles_x * p.tiles_y;
-    const int sat = occ < 2 ? occ : 2;
+    const int full = std::max(1, 512 / (kTile3dY * tile_x));  // blocks of 16 warps
+    const int sat = occ < full ? occ : full;
     const int max_segs = int(ceil_div(zlen, kMinZSeg));
     double best = -1.0;
     long long best_work = 0;
@@ -346,7 +348,7 @@ Layout3d layout3d(int N, int C, int D, int H, int W, int padding)
 {
     const long long planes = (long long)N * C;
     const int Do = out_extent(D, padding), Ho = out_extent(H, padding), Wo = out_extent(W, padding);
-    const long long maxb = planes * ceil_div(Wo, kTile3dX) * ceil_div(Ho, kTile3dY) *
+    const long long maxb = planes * ceil_div(Wo, kStats3dX) * ceil_div(Ho, kTile3dY) *
                            ceil_div(Do, kMinZSeg);
     Layout3d l;
     l.partials_off = kCounterBytes;
@@ -746,7 +748,7 @@ int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
     if (pa.blocks > INT_MAX) return GBSSIM_ESHAPE;
     apply_plan(a, pa);
     a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
@@ -755,7 +757,7 @@ int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H,
     a.blocks_per_image = int(pa.blocks / N);
     cudaError_t e = ssim3d_stats_launch(a, grad, int(pa.blocks), s);
     if (e != cudaSuccess || !grad) return cuda_fail(e);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
     if (pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
     apply_plan(a, pb);
     a.out1 = saved_or_null;
@@ -811,8 +813,8 @@ int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int
                                              size_t(C) * D * H * W, total, d->sm_count, s));
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
     if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
     apply_plan(a, pa);
     a.partials = nullptr;
@@ -918,8 +920,8 @@ int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, d->sm_count, d->occ3d[0]);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, d->sm_count, d->occ3d[1]);
+    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
+    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
     if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
     apply_plan(a, pa);
     a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);

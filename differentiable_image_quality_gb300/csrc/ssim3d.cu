@@ -3,7 +3,8 @@
 //
 // Following that page's plan -- keep the 2D convolution on XY slices, and do
 // the Z convolution and SSIM through a ring buffer, one depth row per thread --
-// a CTA owns an XY tile of 16 x 16 columns and walks along Z one slice per step:
+// a CTA owns an XY tile of 16 x 8 (statistics) or 16 x 16 (adjoint) columns and
+// walks along Z one slice per step:
 //   XY  the slice's row pass and column pass in shared memory (the slice tile
 //       plus its 10-pixel halo staged by tensor copies -- one thread issues
 //       them, a transaction barrier per buffer tracks them, every wait bounded
@@ -31,38 +32,50 @@
 namespace gbssim {
 namespace {
 
-constexpr int NT = kThreads3d;   // 256
-constexpr int TY = kTile3dY;     // 16 rows of columns per tile
-constexpr int TX = kTile3dX;     // 16 columns per row
-constexpr int IY = TY + 10, IX = TX + 10;   // 26 x 26 staged slice tile
-constexpr int IXP = 28;          // float pitch of a staged input row (7 x 16 bytes)
-constexpr int GXP = IX + 1;      // float4 pitch of a staged derivative row (27)
-constexpr int HXP = TX + 1;      // float4 pitch of a row-pass output row (17)
-constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;   // row-pass items per slice (104)
-constexpr int KY = 2, NYG = TY / KY, NYI = NYG * TX;   // column-pass items per slice (128)
-constexpr int NBUF = 6;      // staged slices in flight
+// Tile geometry of a 3D kernel: TY x TX columns, one thread per column.  The
+// statistics kernel runs 16 x 8 tiles (128 threads, four blocks per SM), the
+// adjoint kernel 16 x 16 tiles (256 threads, two blocks per SM): measured on
+// the 128^3 volume, each is the faster shape for its kernel.
+template <int TX_>
+struct Geo {
+    static constexpr int TY = kTile3dY, TX = TX_, NT = TY * TX;
+    static constexpr int IY = TY + 10, IX = TX + 10;  // staged slice tile
+    // float pitch of a staged input row: a multiple of 16 bytes, an odd number of
+    // 16-byte units (28 for 16 columns, 20 for 8)
+    static constexpr int IXU = (IX + 3) / 4, IXP = 4 * (IXU % 2 ? IXU : IXU + 1);
+    static constexpr int GXP = IX + 1;  // float4 pitch of a staged derivative row (odd)
+    static constexpr int HXP = TX + 1;  // float4 pitch of a row-pass output row
+    static constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;  // row-pass items per slice
+    static constexpr int KY = 2, NYG = TY / KY, NYI = NYG * TX;  // column-pass items per slice
+    // staging buffers, each a multiple of 128 bytes (tensor-copy destinations)
+    static constexpr int XSTAGE = (IY * IXP + 31) / 32 * 32;  // floats of a staged input tile
+    static constexpr int GSTAGE = (IY * GXP + 7) / 8 * 8;     // float4 of a staged derivative tile
+    static constexpr int CSTAGE = TY * TX;                     // floats of a chain-rule pixel tile
+    static_assert(TX % KX == 0 && TY % KY == 0, "items tile the columns");
+    static_assert(NYI % 32 == 0, "column-pass items fill whole warps");
+    static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
+    static_assert((CSTAGE * 4) % 128 == 0, "chain tiles stay 128-byte aligned");
+};
+using GS = Geo<kStats3dX>;  // statistics kernel
+using GA = Geo<kAdj3dX>;    // adjoint kernel
+
+constexpr int NBUF = 6;         // staged slices in flight
 constexpr int CBUF = NBUF + 1;  // adjoint: chain-rule pixel tiles in flight
-
-static_assert(NT == TY * TX, "one thread per column of the tile");
-static_assert(NYI % 32 == 0, "column-pass items fill whole warps");
-static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
-
-// Staging buffers, each a multiple of 128 bytes (tensor-copy destinations).
-constexpr int XSTAGE = (IY * IXP + 31) / 32 * 32;  // floats of a staged input tile
-constexpr int GSTAGE = (IY * GXP + 7) / 8 * 8;     // float4 of a staged derivative tile
-constexpr int CSTAGE = TY * TX;                     // floats of a chain-rule pixel tile
-constexpr unsigned kStatsTx = 2u * IY * IXP * sizeof(float);
-constexpr unsigned kAdjTx = unsigned(IY * GXP * sizeof(float4) + 2 * CSTAGE * sizeof(float));
+constexpr unsigned kStatsTx = 2u * GS::IY * GS::IXP * sizeof(float);
+constexpr unsigned kAdjTx =
+    unsigned(GA::IY * GA::GXP * sizeof(float4) + 2 * GA::CSTAGE * sizeof(float));
 constexpr long long kWaitCycles = 1LL << 31;   // staging wait limit (about a second)
 constexpr long long kDrainCycles = 1LL << 27;  // after a failed wait: copies still in flight
 
 __device__ unsigned g_staging3d_status;  // bit 0: a staging wait ran out of time
 
-constexpr size_t kStatsInBytes = size_t(2) * NBUF * XSTAGE * sizeof(float);
-constexpr size_t kAdjInBytes = size_t(NBUF) * GSTAGE * sizeof(float4);
-constexpr size_t kChainBytes = size_t(2) * CBUF * CSTAGE * sizeof(float);
-constexpr size_t kXBytes = size_t(2) * IY * HXP * sizeof(float4);
-constexpr size_t kYBytes = size_t(2) * TY * TX * sizeof(float4);  // two slices
+constexpr size_t kStatsInBytes = size_t(2) * NBUF * GS::XSTAGE * sizeof(float);
+constexpr size_t kStatsXBytes = size_t(2) * GS::IY * GS::HXP * sizeof(float4);
+constexpr size_t kStatsYBytes = size_t(2) * GS::TY * GS::TX * sizeof(float4);  // two slices
+constexpr size_t kAdjInBytes = size_t(NBUF) * GA::GSTAGE * sizeof(float4);
+constexpr size_t kChainBytes = size_t(2) * CBUF * GA::CSTAGE * sizeof(float);
+constexpr size_t kAdjXBytes = size_t(2) * GA::IY * GA::HXP * sizeof(float4);
+constexpr size_t kAdjYBytes = size_t(2) * GA::TY * GA::TX * sizeof(float4);
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
@@ -124,14 +137,17 @@ __device__ __forceinline__ void drain_failed(uint64_t *bars, int waited, int iss
 }
 
 template <bool GRAD>
-__global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const __grid_constant__ Ssim3dArgs a)
+__global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_constant__ Ssim3dArgs a)
 {
+    constexpr int NT = GS::NT, TY = GS::TY, TX = GS::TX, IY = GS::IY, IX = GS::IX,
+                  IXP = GS::IXP, HXP = GS::HXP, KX = GS::KX, NXI = GS::NXI, KY = GS::KY,
+                  NYI = GS::NYI, XSTAGE = GS::XSTAGE;
     extern __shared__ __align__(128) unsigned char smem_dyn[];
     unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
     float *xs = reinterpret_cast<float *>(smem_raw);
     float *ys = xs + NBUF * XSTAGE;
     float4 *hx = reinterpret_cast<float4 *>(smem_raw + kStatsInBytes);
-    float4 *hy = hx + 2 * IY * HXP;
+    float4 *hy = hx + 2 * IY * HXP;  // kStatsXBytes after hx
     __shared__ double red[NT / 32];
     __shared__ uint64_t bars[NBUF];
 
@@ -353,8 +369,11 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_stats_kernel(const __grid_consta
 // ------------------------------------------------------------------ kernel B
 
 template <bool G2>
-__global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
+__global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
 {
+    constexpr int NT = GA::NT, TY = GA::TY, TX = GA::TX, IY = GA::IY, IX = GA::IX,
+                  GXP = GA::GXP, HXP = GA::HXP, KX = GA::KX, NXI = GA::NXI, KY = GA::KY,
+                  NYI = GA::NYI, GSTAGE = GA::GSTAGE, CSTAGE = GA::CSTAGE;
     extern __shared__ __align__(128) unsigned char smem_dyn[];
     unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
     float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][GSTAGE]
@@ -530,18 +549,18 @@ __global__ void __launch_bounds__(NT, 2) ssim3d_adjoint_kernel(const __grid_cons
 }
 
 template <typename K>
-cudaError_t prepare(K kernel, size_t smem, int *occ)
+cudaError_t prepare(K kernel, int threads, size_t smem, int *occ)
 {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kernel, NT, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kernel, threads, smem);
 }
 
 }  // namespace
 
-size_t ssim3d_stats_smem() { return 128 + kStatsInBytes + kXBytes + kYBytes; }
-size_t ssim3d_adjoint_smem() { return 128 + kAdjInBytes + kChainBytes + kXBytes + kYBytes; }
+size_t ssim3d_stats_smem() { return 128 + kStatsInBytes + kStatsXBytes + kStatsYBytes; }
+size_t ssim3d_adjoint_smem() { return 128 + kAdjInBytes + kChainBytes + kAdjXBytes + kAdjYBytes; }
 
 void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes)
 {
@@ -553,7 +572,7 @@ void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes)
         const unsigned long long W = a.W, H = a.H, D = a.D, P = planes;
         const unsigned long long dims[4] = {W, H, D, P};
         const unsigned long long st[3] = {W * 4, H * W * 4, D * H * W * 4};
-        const unsigned bx[4] = {IXP, IY, 1, 1}, bc[4] = {TX, TY, 1, 1};
+        const unsigned bx[4] = {GS::IXP, GS::IY, 1, 1}, bc[4] = {GA::TX, GA::TY, 1, 1};
         ok = encode_tiled_f32(a.tm_x, a.x, 4, dims, st, bx) &&
              encode_tiled_f32(a.tm_y, a.y, 4, dims, st, bx) &&
              encode_tiled_f32(a.tm_cx, a.x, 4, dims, st, bc) &&
@@ -563,7 +582,7 @@ void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes)
         const unsigned long long Wo = a.Wo, Ho = a.Ho, Do = a.Do, P = planes;
         const unsigned long long dims[4] = {4 * Wo, Ho, Do, P};
         const unsigned long long st[3] = {Wo * 16, Ho * Wo * 16, Do * Ho * Wo * 16};
-        const unsigned bg[4] = {4 * GXP, IY, 1, 1};
+        const unsigned bg[4] = {4 * GA::GXP, GA::IY, 1, 1};
         ok = a.gfield && encode_tiled_f32(a.tm_g, a.gfield, 4, dims, st, bg);
     }
     a.tma = ok ? 1 : 0;
@@ -584,10 +603,11 @@ cudaError_t ssim3d_prepare(int occ[2])
 {
     int o[4] = {0, 0, 0, 0};
     cudaError_t e;
-    if ((e = prepare(ssim3d_stats_kernel<false>, ssim3d_stats_smem(), &o[0])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_stats_kernel<true>, ssim3d_stats_smem(), &o[1])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_adjoint_kernel<false>, ssim3d_adjoint_smem(), &o[2])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_adjoint_kernel<true>, ssim3d_adjoint_smem(), &o[3])) != cudaSuccess) return e;
+    const size_t ss = ssim3d_stats_smem(), sa = ssim3d_adjoint_smem();
+    if ((e = prepare(ssim3d_stats_kernel<false>, GS::NT, ss, &o[0])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_stats_kernel<true>, GS::NT, ss, &o[1])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_adjoint_kernel<false>, GA::NT, sa, &o[2])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_adjoint_kernel<true>, GA::NT, sa, &o[3])) != cudaSuccess) return e;
     occ[0] = o[0] < o[1] ? o[0] : o[1];
     occ[1] = o[2] < o[3] ? o[2] : o[3];
     return (occ[0] < 1 || occ[1] < 1) ? cudaErrorInvalidConfiguration : cudaSuccess;
@@ -596,18 +616,18 @@ cudaError_t ssim3d_prepare(int occ[2])
 cudaError_t ssim3d_stats_launch(const Ssim3dArgs &a, bool grad, int blocks, cudaStream_t s)
 {
     if (grad)
-        ssim3d_stats_kernel<true><<<blocks, NT, ssim3d_stats_smem(), s>>>(a);
+        ssim3d_stats_kernel<true><<<blocks, GS::NT, ssim3d_stats_smem(), s>>>(a);
     else
-        ssim3d_stats_kernel<false><<<blocks, NT, ssim3d_stats_smem(), s>>>(a);
+        ssim3d_stats_kernel<false><<<blocks, GS::NT, ssim3d_stats_smem(), s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t ssim3d_adjoint_launch(const Ssim3dArgs &a, bool g2, int blocks, cudaStream_t s)
 {
     if (g2)
-        ssim3d_adjoint_kernel<true><<<blocks, NT, ssim3d_adjoint_smem(), s>>>(a);
+        ssim3d_adjoint_kernel<true><<<blocks, GA::NT, ssim3d_adjoint_smem(), s>>>(a);
     else
-        ssim3d_adjoint_kernel<false><<<blocks, NT, ssim3d_adjoint_smem(), s>>>(a);
+        ssim3d_adjoint_kernel<false><<<blocks, GA::NT, ssim3d_adjoint_smem(), s>>>(a);
     return cudaGetLastError();
 }
 

@@ -7,9 +7,9 @@
 
 namespace gbssim {
 
-constexpr int kThreads3d = 256;
-constexpr int kTile3dY = 16;  // tile rows (one thread per column of the tile)
-constexpr int kTile3dX = 16;
+constexpr int kTile3dY = 16;   // tile rows (one thread per column of the tile)
+constexpr int kStats3dX = 8;   // statistics kernel tiles: 16 x 8 columns (output domain)
+constexpr int kAdj3dX = 16;    // adjoint kernel tiles: 16 x 16 columns (volume)
 
 // Arguments of both 3D kernels.  Grid: one block per (plane, z segment, tile
 // row, tile column), flattened with the tile column fastest.  The statistics
