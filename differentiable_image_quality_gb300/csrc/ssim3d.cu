@@ -113,6 +113,35 @@ __device__ __forceinline__ void taps4(const float4 *src, int stride, float2 (&oa
     }
 }
 
+// The same pass over the first three components only (x, y as a pair, z
+// alone): the adjoint for grad_img1 needs B^T of g_mu1, g_e and g_e12, not g_mu2.
+template <int K>
+__device__ __forceinline__ void taps3(const float4 *src, int stride, float2 (&oa)[K], float (&oc)[K])
+{
+#pragma unroll
+    for (int m = 0; m < K + 10; ++m) {
+        const float4 v = src[m * stride];
+#pragma unroll
+        for (int o = 0; o < K; ++o) {
+            const int t = m - o;
+            if (t < 0 || t > 10) continue;
+            oa[o] = (t == 0) ? __fmul2_rn(splat(tap(t)), lo(v)) : __ffma2_rn(splat(tap(t)), lo(v), oa[o]);
+            oc[o] = (t == 0) ? tap(t) * v.z : fmaf(tap(t), v.z, oc[o]);
+        }
+    }
+}
+
+// sum_a w_a r[(N + 1 + a) % 11] for a scalar ring.
+template <int N>
+__device__ __forceinline__ float ring_sum1(const float (&r)[kTaps])
+{
+    float acc = tap(5) * r[(N + 6) % kTaps];
+#pragma unroll
+    for (int a = 0; a < 5; ++a)
+        acc = fmaf(tap(a), r[(N + 1 + a) % kTaps] + r[(N + 11 - a) % kTaps], acc);
+    return acc;
+}
+
 // Z-step dispatch: the ring slot is a compile-time constant in each case.
 #define GBSSIM_RING_SWITCH(s, CALL)                                           \
     switch ((s) % kTaps) {                                                    \
@@ -437,10 +466,20 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     };
 
     // adjoint row pass: gradient columns [KX g, KX g + KX) of staged row r
+    // (grad_img1 only: the fourth component, g_mu2, is not blurred; its slot
+    // carries zero)
     auto x_item = [&](int s, int item) {
         const int g = item / IY, r = item - g * IY;
         float2 oa[KX], ob[KX];
-        taps4<KX>(gs + (s % NBUF) * GSTAGE + r * GXP + g * KX, 1, oa, ob);
+        const float4 *src = gs + (s % NBUF) * GSTAGE + r * GXP + g * KX;
+        if (G2) {
+            taps4<KX>(src, 1, oa, ob);
+        } else {
+            float oc[KX];
+            taps3<KX>(src, 1, oa, oc);
+#pragma unroll
+            for (int o = 0; o < KX; ++o) ob[o] = f2(oc[o], 0.f);
+        }
         float4 *dst = ux + ((s & 1) * IY + r) * HXP + g * KX;
 #pragma unroll
         for (int o = 0; o < KX; ++o) dst[o] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
@@ -449,7 +488,15 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     auto y_item = [&](int s, int item) {
         const int g = item / TX, tx = item - g * TX;
         float2 oa[KY], ob[KY];
-        taps4<KY>(ux + ((s & 1) * IY + g * KY) * HXP + tx, HXP, oa, ob);
+        const float4 *src = ux + ((s & 1) * IY + g * KY) * HXP + tx;
+        if (G2) {
+            taps4<KY>(src, HXP, oa, ob);
+        } else {
+            float oc[KY];
+            taps3<KY>(src, HXP, oa, oc);
+#pragma unroll
+            for (int o = 0; o < KY; ++o) ob[o] = f2(oc[o], 0.f);
+        }
 #pragma unroll
         for (int o = 0; o < KY; ++o)
             uy[((s & 1) * TY + g * KY + o) * TX + tx] = make_float4(oa[o].x, oa[o].y, ob[o].x, ob[o].y);
@@ -458,24 +505,34 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     const int ty = tid / TX, tx = tid - ty * TX;
     const int qy = y0 + ty, qx = x0 + tx;
     const bool col_ok = (qy < a.H) && (qx < a.W);
-    float2 rA[kTaps], rB[kTaps];
+    float2 rA[kTaps], rB[kTaps];  // rB: (g_e12, g_mu2) with grad_img2
+    float rC[kTaps];               // g_e12 alone otherwise
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) rA[k] = rB[k] = f2(0.f, 0.f);
+    for (int k = 0; k < kTaps; ++k) {
+        rA[k] = rB[k] = f2(0.f, 0.f);
+        rC[k] = 0.f;
+    }
 
     auto z_step = [&](auto K_, int s) {
         constexpr int K = decltype(K_)::value;
         const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
         rA[K] = lo(h);
-        rB[K] = hi(h);
+        if (G2) rB[K] = hi(h);
+        else rC[K] = h.z;
         const int q = q0 + s - 10;
         if (s >= 10 && q < q1 && col_ok) {
             const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
             const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
             const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
             const float2 vA = ring_sum2<K>(rA);  // (B^T g_m1, B^T g_e)
-            const float2 vB = ring_sum2<K>(rB);  // (B^T g_e12, B^T g_m2)
-            a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
-            if (G2) a.out2[gi] = scale * fmaf(2.0f * y, vA.y, fmaf(x, vB.x, vB.y));
+            if (G2) {
+                const float2 vB = ring_sum2<K>(rB);  // (B^T g_e12, B^T g_m2)
+                a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
+                a.out2[gi] = scale * fmaf(2.0f * y, vA.y, fmaf(x, vB.x, vB.y));
+            } else {
+                const float v12 = ring_sum1<K>(rC);  // B^T g_e12
+                a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, v12, vA.x));
+            }
         }
     };
 #define GBSSIM_ZB(K) z_step(std::integral_constant<int, K>{}, s)
