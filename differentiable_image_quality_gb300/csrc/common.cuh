@@ -261,58 +261,21 @@ __device__ __forceinline__ double block_sum(float v, double *scratch /* NT/32 do
     return t;
 }
 
-// Grid-wide finish of the per-image means.  Every block calls this once, with
-// its partial sum already written to partials[blockIdx.x] by thread 0.  The
-// last block to arrive sums each image's partials (double, a fixed assignment of
-// partials to threads and a fixed-order block reduction: deterministic) and
-// writes mean[n] = sum / count, then resets the counter to zero for the next
-// call.  blocks_per_image consecutive blocks belong to one image.
-template <int NT>
-__device__ __forceinline__ void finish_means(double *partials, unsigned *counter, float *mean,
-                                             int images, int blocks_per_image, double count)
-{
-    __shared__ bool last;
-    __shared__ double wsum[NT / 32];
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned total = gridDim.x;
-        const unsigned ticket = atomicAdd(counter, 1u);
-        last = (ticket == total - 1);
-    }
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int n = 0; n < images; ++n) {
-        const double *p = partials + static_cast<size_t>(n) * blocks_per_image;
-        double s = 0.0;
-        for (int b = threadIdx.x; b < blocks_per_image; b += NT) s += __ldcg(p + b);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-        if (lane == 0) wsum[warp] = s;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double t = 0.0;
-#pragma unroll
-            for (int w = 0; w < NT / 32; ++w) t += wsum[w];
-            mean[n] = static_cast<float>(t / count);
-        }
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) *counter = 0u;
-}
-
-// finish_means for K quantities at once: partials holds K arrays of `stride`
-// doubles (this block's sums already written at each), mean holds K arrays of
-// `images` floats.  One completion ticket per block; the last block reduces
-// every quantity of every image in the same fixed order as finish_means.
+// Grid-wide finish of per-image means.  Every block calls this once, with its
+// partial sums already written (and fenced) at partials[k * stride + slot],
+// k < K.  The last block to arrive reduces, for every quantity k and image n,
+// the blocks_per_image consecutive partials of that image -- one warp per
+// (k, n), its lanes striding the partials, then a fixed shuffle tree: a fixed
+// order, so the result is deterministic -- and writes
+// mean[k * images + n] = sum / count.  It then resets the counter to zero for
+// the next call.  The (k, n) reductions run in parallel: each costs one round
+// of L2 loads.
 template <int NT, int K>
 __device__ __forceinline__ void finish_means_k(double *partials, int stride, unsigned *counter,
                                                float *mean, int images, int blocks_per_image,
                                                double count)
 {
     __shared__ bool last;
-    __shared__ double wsum[NT / 32];
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned ticket = atomicAdd(counter, 1u);
@@ -322,25 +285,24 @@ __device__ __forceinline__ void finish_means_k(double *partials, int stride, uns
     if (!last) return;
     __threadfence();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int k = 0; k < K; ++k) {
-        for (int n = 0; n < images; ++n) {
-            const double *p = partials + size_t(k) * stride + size_t(n) * blocks_per_image;
-            double s = 0.0;
-            for (int b = threadIdx.x; b < blocks_per_image; b += NT) s += __ldcg(p + b);
+    for (int q = warp; q < K * images; q += NT / 32) {
+        const int k = q / images, n = q - k * images;
+        const double *p = partials + size_t(k) * stride + size_t(n) * blocks_per_image;
+        double s = 0.0;
+        for (int b = lane; b < blocks_per_image; b += 32) s += __ldcg(p + b);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-            if (lane == 0) wsum[warp] = s;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                double t = 0.0;
-#pragma unroll
-                for (int w = 0; w < NT / 32; ++w) t += wsum[w];
-                mean[k * images + n] = static_cast<float>(t / count);
-            }
-            __syncthreads();
-        }
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) mean[k * images + n] = static_cast<float>(s / count);
     }
     if (threadIdx.x == 0) *counter = 0u;
+}
+
+// One quantity: partials[slot], mean[n].
+template <int NT>
+__device__ __forceinline__ void finish_means(double *partials, unsigned *counter, float *mean,
+                                             int images, int blocks_per_image, double count)
+{
+    finish_means_k<NT, 1>(partials, 0, counter, mean, images, blocks_per_image, count);
 }
 
 }  // namespace gbssim

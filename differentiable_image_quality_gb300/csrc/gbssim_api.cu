@@ -17,7 +17,8 @@ namespace {
 using namespace gbssim;
 
 constexpr int kMaxDevices = 64;
-constexpr int kMinSegRows = 22;    // shortest row segment the planner uses
+constexpr int kMinSegRows = 22;    // shortest row segment of a gradient-mode plan
+constexpr int kMinSegRowsFwd = 11; // ... and of a forward-only plan (small images: more blocks)
 constexpr size_t kCounterBytes = 256;  // completion counter, then the partial sums
 
 struct DeviceInfo {
@@ -184,7 +185,7 @@ Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad
     const int halo = grad ? 20 : 10;
     const int S = ssim2d_strips(grad, W, Wo, off);
     p.strips = S;
-    const int max_segs = std::max(1, rows / kMinSegRows);
+    const int max_segs = std::max(1, rows / (grad ? kMinSegRows : kMinSegRowsFwd));
     auto take = [&](int per_plane) {
         p.per_plane = per_plane;
         p.base = per_plane / S;
@@ -269,11 +270,11 @@ void set_segments(Ssim2dArgs &a, const Plan2d &p, int rows)
     a.long_blocks = int(p.long_blocks);
 }
 
-// Upper bound of blocks over every plan (segments never shorter than kMinSegRows).
+// Upper bound of blocks over every plan (segments never shorter than the minima).
 long long max_blocks2d(long long planes, int H, int W, int Ho, int Wo, int off)
 {
     const long long g = ssim2d_strips(true, W, Wo, off) * ceil_div(H, kMinSegRows);
-    const long long f = ssim2d_strips(false, W, Wo, off) * ceil_div(Ho, kMinSegRows);
+    const long long f = ssim2d_strips(false, W, Wo, off) * ceil_div(Ho, kMinSegRowsFwd);
     return planes * (g > f ? g : f);
 }
 

@@ -770,31 +770,34 @@ cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
 
 // Both images one octave down: out(i, j) = mean of the in-range pixels of the
 // 2x2 block at (2i, 2j); planes of H x W -> Hd x Wd = ceil(H/2) x ceil(W/2).
+// Block b handles output rows b, b + gridDim.x, ... (row = plane * Hd + i).
 __global__ void __launch_bounds__(256) downscale2x_kernel(const float *__restrict__ x,
                                                           const float *__restrict__ y,
                                                           float *__restrict__ ox,
                                                           float *__restrict__ oy, int H, int W,
-                                                          size_t total)
+                                                          long long rows)
 {
     const int Hd = (H + 1) >> 1, Wd = (W + 1) >> 1;
-    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += size_t(gridDim.x) * blockDim.x) {
-        const int j = int(i % size_t(Wd));
-        const size_t t = i / size_t(Wd);
-        const int r = int(t % size_t(Hd));
-        const size_t plane = t / size_t(Hd);
-        const int r0 = 2 * r, c0 = 2 * j;
-        const bool r1 = r0 + 1 < H, c1 = c0 + 1 < W;
-        const size_t b = (plane * size_t(H) + r0) * size_t(W) + c0;
-        float sx = x[b], sy = y[b];
-        if (c1) { sx += x[b + 1]; sy += y[b + 1]; }
-        if (r1) {
-            sx += x[b + W]; sy += y[b + W];
-            if (c1) { sx += x[b + W + 1]; sy += y[b + W + 1]; }
+    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+        const long long plane = row / Hd;
+        const int i = int(row - plane * Hd);
+        const int r0 = 2 * i;
+        const bool r1 = r0 + 1 < H;
+        const float *px = x + (plane * H + r0) * W, *py = y + (plane * H + r0) * W;
+        float *qx = ox + row * Wd, *qy = oy + row * Wd;
+        for (int j = threadIdx.x; j < Wd; j += blockDim.x) {
+            const int c0 = 2 * j;
+            const bool c1 = c0 + 1 < W;
+            float sx = px[c0], sy = py[c0];
+            if (c1) { sx += px[c0 + 1]; sy += py[c0 + 1]; }
+            if (r1) {
+                sx += px[W + c0]; sy += py[W + c0];
+                if (c1) { sx += px[W + c0 + 1]; sy += py[W + c0 + 1]; }
+            }
+            const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
+            qx[j] = sx * inv;
+            qy[j] = sy * inv;
         }
-        const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
-        ox[i] = sx * inv;
-        oy[i] = sy * inv;
     }
 }
 
@@ -878,12 +881,10 @@ const void *ssim2d_components_kernel_ptr()
 cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
                                long long planes, int H, int W, int sm_count, cudaStream_t s)
 {
-    const size_t total = size_t(planes) * size_t((H + 1) / 2) * size_t((W + 1) / 2);
-    size_t blocks = (total + 255) / 256;
-    const size_t cap = size_t(sm_count) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    downscale2x_kernel<<<unsigned(blocks), 256, 0, s>>>(x, y, ox, oy, H, W, total);
+    const long long rows = planes * ((H + 1) / 2);
+    const long long cap = (long long)sm_count * 8;
+    const unsigned blocks = unsigned(rows < cap ? rows : cap);
+    downscale2x_kernel<<<blocks, 256, 0, s>>>(x, y, ox, oy, H, W, rows);
     return cudaGetLastError();
 }
 

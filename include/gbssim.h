@@ -144,7 +144,7 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
  * library, held until the process exits.  It allocates nothing.
  *   - Shapes whose workspace (gbssim_workspace_bytes) would exceed that array
  *     return GBSSIM_ETOOLARGE; use ssim_fwd for them.  A 1 x 3 x 1080 x 1920
- *     pair needs about 20 KB of it.
+ *     pair needs about 35 KB of it.
  *   - All calls on a device share the one array and it keeps the previous
  *     call's contents; the call clears the part that must start at zero.  Calls
  *     whose work overlaps on the GPU (other streams, other threads) race on it:
