@@ -40,6 +40,7 @@ NOMINAL_HBM_GBS = 8000.0
 FLUSH_BYTES = 256 << 20
 KERNEL_NAME = "ssim2d_stream_kernel<true,false>"
 PROFILE = os.path.join(ROOT, "profiles", "ssim2d_grad_splat1080_valid.md")
+PROFILE3D = os.path.join(ROOT, "profiles", "ssim3d_volume128_valid.md")
 
 # Algorithmic float32 operations of the gradient-mode kernel per input pixel
 # (fused forward statistics, SSIM derivatives, adjoint and chain rule), counting
@@ -271,12 +272,12 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the gradient kernel from the committed ncu
+def profiled_traffic(path=PROFILE):
+    """DRAM bytes per launch of the profiled kernel(s) from a committed ncu
     summary, if it was taken from the current kernel sources; else None."""
-    if not os.path.exists(PROFILE):
+    if not os.path.exists(path):
         return None
-    text = open(PROFILE).read()
+    text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     if not m or not s or s.group(1) != kernel_source_digest():
@@ -500,7 +501,8 @@ def run_ours(args):
         "roofline": {"kernel": KERNEL_NAME if not is3d else KERNEL3D_NAME, "bound": "alu",
                      "achieved": achieved_tflops, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved_tflops / alu_peak_tflops,
-                     "traffic": profiled_traffic() if (name == WORKLOAD) else None,
+                     "traffic": (profiled_traffic() if name == WORKLOAD else
+                                 profiled_traffic(PROFILE3D) if name == "volume128_valid" else None),
                      "peak_basis": f"{sm_count} SMs x 128 fp32 lanes x 2 flops x {sm_max:.0f} MHz",
                      "flops_per_pixel": flops_px},
         "hbm_roofline": {"min_bytes_per_step": min_bytes, "achieved_gbs": hbm_gbs,
