@@ -244,9 +244,15 @@ def ssim_pyramid(img1, img2, padding, octaves: int, want_maps: bool = False, out
         workspace = _workspace(img1.device, need)
     if out_means is None:
         out_means = torch.empty((int(octaves), 3, N), dtype=torch.float32, device=img1.device)
+    nf = int(lib.gbssim_pyramid_map_floats(N, C, H, W, pad, int(octaves)))
     if maps is None and want_maps:
-        nf = int(lib.gbssim_pyramid_map_floats(N, C, H, W, pad, int(octaves)))
         maps = torch.empty(nf, dtype=torch.float32, device=img1.device)
+    if maps is not None and (maps.numel() < nf or maps.dtype != torch.float32
+                             or not maps.is_contiguous() or maps.device != img1.device):
+        raise ValueError(f"maps must be a contiguous float32 tensor of at least {nf} elements "
+                         f"on {img1.device}")
+    if out_means.shape != (int(octaves), 3, N) or out_means.dtype != torch.float32:
+        raise ValueError(f"out_means must be a float32 tensor of shape ({int(octaves)}, 3, {N})")
     st = lib.ssim_pyramid(_abi.ptr(img1), _abi.ptr(img2), N, C, H, W, pad, int(octaves),
                           _abi.ptr(out_means), _abi.ptr(maps), _abi.ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(img1))

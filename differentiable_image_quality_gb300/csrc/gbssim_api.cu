@@ -632,7 +632,9 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
         overlaps(out_means, mean_bytes, img1, img_bytes) ||
         overlaps(out_means, mean_bytes, img2, img_bytes) ||
         overlaps(workspace, workspace_bytes, img1, img_bytes) ||
-        overlaps(workspace, workspace_bytes, img2, img_bytes))
+        overlaps(workspace, workspace_bytes, img2, img_bytes) ||
+        overlaps(workspace, workspace_bytes, out_means, mean_bytes) ||
+        overlaps(workspace, workspace_bytes, maps_or_null, map_bytes))
         return GBSSIM_EINVAL;
 
     DeviceInfo *d = nullptr;

@@ -183,3 +183,4 @@ def test_pyramid_sizes_and_argument_errors(lib):
     assert pyr(wsb=ws - 1) == EWORKSPACE
     assert pyr(wsp=FAKE * 256 + 16) == EWORKSPACE
     assert pyr(maps=(1 << 30) + 64) == EINVAL  # maps overlapping img1
+    assert pyr(wsp=3 << 30) == EINVAL             # workspace overlapping the means
