@@ -2,7 +2,7 @@
 // 2D with an 11x11x11 separable window on NCDHW volumes.
 //
 // Following that page's plan -- keep the 2D convolution on XY slices, and do
-// the Z convolution and SSIM through a ring buffer, one depth row per thread --
+// the Z convolution and SSIM per depth row, one depth row per thread --
 // a CTA owns an XY tile of 16 x 8 (statistics) or 16 x 16 (adjoint) columns and
 // walks along Z one slice per step:
 //   XY  the slice's row pass and column pass in shared memory (the slice tile
@@ -11,8 +11,9 @@
 //       -- or by cp.async where the tile does not start on a 16-byte column;
 //       NBUF buffers, a slice's copies issued NBUF - 3 steps before it is
 //       waited for);
-//   Z   each thread keeps an 11-slice register ring of its column's XY-blurred
-//       values; the ring's weighted sum is the full 3D window.
+//   Z   each thread keeps, in registers, the partial sums of the ten Z windows
+//       its column has open (a shift register); each new XY-blurred slice
+//       completes one window and advances the others.
 // Two kernels:
 //   stats    statistics -> SSIM (mean, map) and, for gradients, the derivatives
 //            of SSIM with respect to the four shifted moments, one float4 per
@@ -82,18 +83,6 @@ __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
 __device__ __forceinline__ float2 lo(const float4 &v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi(const float4 &v) { return make_float2(v.z, v.w); }
 
-// sum_a w_a r[(N + 1 + a) % 11] (the oldest entry gets w_0), symmetric taps.
-template <int N>
-__device__ __forceinline__ float2 ring_sum2(const float2 (&r)[kTaps])
-{
-    float2 acc = __fmul2_rn(splat(tap(5)), r[(N + 6) % kTaps]);
-#pragma unroll
-    for (int a = 0; a < 5; ++a)
-        acc = __ffma2_rn(splat(tap(a)), __fadd2_rn(r[(N + 1 + a) % kTaps], r[(N + 11 - a) % kTaps]),
-                         acc);
-    return acc;
-}
-
 // 11-tap pass over float4 values loaded from smem at src[stride * m],
 // m = 0 .. K + 9, giving K outputs (two float pairs each).
 template <int K>
@@ -131,25 +120,30 @@ __device__ __forceinline__ void taps3(const float4 *src, int stride, float2 (&oa
     }
 }
 
-// sum_a w_a r[(N + 1 + a) % 11] for a scalar ring.
-template <int N>
-__device__ __forceinline__ float ring_sum1(const float (&r)[kTaps])
+// The Z pass as a shift register of pending window sums.  P[j] holds, after
+// slice s, the part of the window that completes at slice s + j + 1 contributed
+// by slices <= s.  Slice s with value h completes the window of P[0] (h is its
+// newest slice, weight w_10) and shifts the rest:
+//   out = P[0] + w_10 h,  P[j] = P[j + 1] + w_{9-j} h (j < 9),  P[9] = w_0 h.
+// Every register index is fixed, so no step dispatches on s % 11, and the 11
+// updates are independent.  Same sum as the symmetric ring, other order.
+__device__ __forceinline__ float2 zshift2(float2 (&P)[kTaps - 1], float2 h)
 {
-    float acc = tap(5) * r[(N + 6) % kTaps];
+    const float2 out = __ffma2_rn(splat(tap(10)), h, P[0]);
 #pragma unroll
-    for (int a = 0; a < 5; ++a)
-        acc = fmaf(tap(a), r[(N + 1 + a) % kTaps] + r[(N + 11 - a) % kTaps], acc);
-    return acc;
+    for (int j = 0; j < kTaps - 2; ++j) P[j] = __ffma2_rn(splat(tap(9 - j)), h, P[j + 1]);
+    P[kTaps - 2] = __fmul2_rn(splat(tap(0)), h);
+    return out;
 }
 
-// Z-step dispatch: the ring slot is a compile-time constant in each case.
-#define GBSSIM_RING_SWITCH(s, CALL)                                           \
-    switch ((s) % kTaps) {                                                    \
-    case 0: CALL(0); break;  case 1: CALL(1); break;  case 2: CALL(2); break; \
-    case 3: CALL(3); break;  case 4: CALL(4); break;  case 5: CALL(5); break; \
-    case 6: CALL(6); break;  case 7: CALL(7); break;  case 8: CALL(8); break; \
-    case 9: CALL(9); break;  default: CALL(10); break;                        \
-    }
+__device__ __forceinline__ float zshift1(float (&P)[kTaps - 1], float h)
+{
+    const float out = fmaf(tap(10), h, P[0]);
+#pragma unroll
+    for (int j = 0; j < kTaps - 2; ++j) P[j] = fmaf(tap(9 - j), h, P[j + 1]);
+    P[kTaps - 2] = tap(0) * h;
+    return out;
+}
 
 // ------------------------------------------------------------------ kernel A
 
@@ -286,20 +280,18 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     const int ty = tid / TX, tx = tid - ty * TX;
     const int py = y0 + ty, px = x0 + tx;
     const bool col_ok = (py < a.Ho) && (px < a.Wo);
-    float2 rA[kTaps], rB[kTaps];
+    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, e12)
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) rA[k] = rB[k] = f2(0.f, 0.f);
+    for (int k = 0; k < kTaps - 1; ++k) PA[k] = PB[k] = f2(0.f, 0.f);
     float ssum = 0.0f;
 
-    // Z step: push this column's XY-blurred value of slice s, finish slice s - 10.
-    auto z_step = [&](auto K_, int s) {
-        constexpr int K = decltype(K_)::value;
+    // Z step: this column's XY-blurred value of slice s completes the window of
+    // output slice s - 10.
+    auto z_step = [&](int s) {
         const float4 h = hy[((s & 1) * TY + ty) * TX + tx];
-        rA[K] = lo(h);
-        rB[K] = hi(h);
+        const float2 M = zshift2(PA, lo(h)), E = zshift2(PB, hi(h));
         const int p = z0 + s - 10;
         if (s >= 10 && p < z1 && col_ok) {
-            const float2 M = ring_sum2<K>(rA), E = ring_sum2<K>(rB);
             const Moments mo{M.x, M.y, E.x, E.y};
             float S;
             const size_t oi = ((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px;
@@ -314,7 +306,6 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
             if (a.map) a.map[oi] = S;
         }
     };
-#define GBSSIM_ZA(K) z_step(std::integral_constant<int, K>{}, s)
 
     // Pipeline: step s runs the Z pass of slice s, the column pass of slice
     // s + 1 and the row pass of slice s + 2, then one barrier.  The row and
@@ -364,7 +355,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
-        GBSSIM_RING_SWITCH(s, GBSSIM_ZA)
+        z_step(s);
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
         for (int i = tid; i < ny + nx; i += NT) {
@@ -384,7 +375,6 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
         }
         waited = min(nz, s + 4);
     }
-#undef GBSSIM_ZA
     cp_async_wait<0>();
     if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
 
@@ -505,37 +495,34 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     const int ty = tid / TX, tx = tid - ty * TX;
     const int qy = y0 + ty, qx = x0 + tx;
     const bool col_ok = (qy < a.H) && (qx < a.W);
-    float2 rA[kTaps], rB[kTaps];  // rB: (g_e12, g_mu2) with grad_img2
-    float rC[kTaps];               // g_e12 alone otherwise
+    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (g_m1, g_e), (g_e12, g_mu2)
+    float PC[kTaps - 1];                 // of g_e12 alone without grad_img2
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-        rA[k] = rB[k] = f2(0.f, 0.f);
-        rC[k] = 0.f;
+    for (int k = 0; k < kTaps - 1; ++k) {
+        PA[k] = PB[k] = f2(0.f, 0.f);
+        PC[k] = 0.f;
     }
 
-    auto z_step = [&](auto K_, int s) {
-        constexpr int K = decltype(K_)::value;
+    auto z_step = [&](int s) {
         const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
-        rA[K] = lo(h);
-        if (G2) rB[K] = hi(h);
-        else rC[K] = h.z;
+        const float2 vA = zshift2(PA, lo(h));  // (B^T g_m1, B^T g_e)
+        float2 vB = f2(0.f, 0.f);              // (B^T g_e12, B^T g_m2)
+        float v12 = 0.f;                       // B^T g_e12
+        if (G2) vB = zshift2(PB, hi(h));
+        else v12 = zshift1(PC, h.z);
         const int q = q0 + s - 10;
         if (s >= 10 && q < q1 && col_ok) {
             const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
             const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
             const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
-            const float2 vA = ring_sum2<K>(rA);  // (B^T g_m1, B^T g_e)
             if (G2) {
-                const float2 vB = ring_sum2<K>(rB);  // (B^T g_e12, B^T g_m2)
                 a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
                 a.out2[gi] = scale * fmaf(2.0f * y, vA.y, fmaf(x, vB.x, vB.y));
             } else {
-                const float v12 = ring_sum1<K>(rC);  // B^T g_e12
                 a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, v12, vA.x));
             }
         }
     };
-#define GBSSIM_ZB(K) z_step(std::integral_constant<int, K>{}, s)
 
     // The pipeline of the statistics kernel.  Chain buffer (s + NBUF) % CBUF,
     // filled at step s, held slice s - 1's pixels, read by the Z pass of the
@@ -580,7 +567,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
-        GBSSIM_RING_SWITCH(s, GBSSIM_ZB)
+        z_step(s);
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
         for (int i = tid; i < ny + nx; i += NT) {
@@ -600,7 +587,6 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
         }
         waited = min(nz, s + 4);
     }
-#undef GBSSIM_ZB
     cp_async_wait<0>();
     if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
 }
