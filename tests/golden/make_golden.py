@@ -53,6 +53,19 @@ def case_3d(name, x, y, padding, dL, n_idx=16, seed=0):
     }
 
 
+def case_pyramid(name, x, y, padding, octaves, n_idx=12, seed=0):
+    means, maps = oracle.ssim2d_pyramid(x, y, padding, octaves, want_maps=True)
+    rng = np.random.default_rng(seed)
+    picks = []
+    for o in range(octaves):
+        idx = np.sort(rng.choice(maps[o].size, n_idx, replace=False))
+        picks.append({"idx": idx.tolist(), "values": maps[o].reshape(-1)[idx].tolist()})
+    return {
+        "name": name, "kind": "pyramid", "shape": list(x.shape), "padding": padding,
+        "inputs": name, "octaves": octaves, "means": means.reshape(-1).tolist(), "maps": picks,
+    }
+
+
 def lock_inputs(name):
     """Inputs of each locked case, regenerated from their seeds."""
     if name == "tiny64_valid":
@@ -63,6 +76,10 @@ def lock_inputs(name):
         return uniform_pair((1, 1, 12, 14, 13), 78, std=0.05)
     if name == "uniform_1x2x9x8x10_same":
         return uniform_pair((1, 2, 9, 8, 10), 79, std=0.05)
+    if name == "uniform_2x2x45x50_pyramid":
+        return uniform_pair((2, 2, 45, 50), 80, std=0.07)
+    if name == "uniform_1x1x13x9_pyramid":
+        return uniform_pair((1, 1, 13, 9), 81, std=0.07)
     raise KeyError(name)
 
 
@@ -76,6 +93,10 @@ def main():
     cases.append(case_3d("uniform_1x1x12x14x13_valid", x, y, "valid", [-1.0]))
     x, y = lock_inputs("uniform_1x2x9x8x10_same")
     cases.append(case_3d("uniform_1x2x9x8x10_same", x, y, "same", [-1.0]))
+    x, y = lock_inputs("uniform_2x2x45x50_pyramid")
+    cases.append(case_pyramid("uniform_2x2x45x50_pyramid", x, y, "valid", 3))
+    x, y = lock_inputs("uniform_1x1x13x9_pyramid")
+    cases.append(case_pyramid("uniform_1x1x13x9_pyramid", x, y, "same", 4))
     with open(OUT, "w") as f:
         json.dump({"generator": "tests/golden/make_golden.py", "cases": cases}, f, indent=1)
     print("wrote", OUT)
