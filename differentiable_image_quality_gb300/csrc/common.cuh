@@ -145,6 +145,13 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *map, int x, i
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the kernel ahead of it on the stream has
+// finished, once every block of that kernel has called pdl_trigger (or
+// exited); it must call pdl_wait before touching that kernel's results.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Approximate reciprocal (the hardware instruction, relative error ~1 ulp).
 // Its argument here is a product of two sums each >= C1 or C2, never zero,
 // infinite or subnormal.

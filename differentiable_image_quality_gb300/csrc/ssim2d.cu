@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     __shared__ double red[COMP ? 3 : 1][NT / 32];
     __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
+    pdl_trigger();
     const int tid = threadIdx.x;
     const SegWork w = segment_of(a, blockIdx.x);
     const int strip = w.strip, seg = w.seg, plane = w.plane;
@@ -698,6 +699,7 @@ __global__ void __launch_bounds__(256) scale_fields_vec4(const float4 *f1, const
                                                          float inv_count, size_t per_image4,
                                                          size_t total4)
 {
+    pdl_wait();
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
          i += size_t(gridDim.x) * blockDim.x) {
         const float s = dL[i / per_image4] * inv_count;
@@ -718,6 +720,7 @@ __global__ void __launch_bounds__(256) scale_fields_scalar(const float *f1, cons
                                                            float inv_count, size_t per_image,
                                                            size_t total)
 {
+    pdl_wait();
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += size_t(gridDim.x) * blockDim.x) {
         const float s = dL[i / per_image] * inv_count;
@@ -906,15 +909,23 @@ cudaError_t scale_fields_launch(const float *f1, const float *f2, float *g1, flo
     const size_t cap = size_t(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (vec)
-        scale_fields_vec4<<<unsigned(blocks), 256, 0, s>>>(
-            reinterpret_cast<const float4 *>(f1), reinterpret_cast<const float4 *>(f2),
-            reinterpret_cast<float4 *>(g1), reinterpret_cast<float4 *>(g2), dL, inv_count,
-            per_image / 4, total / 4);
-    else
-        scale_fields_scalar<<<unsigned(blocks), 256, 0, s>>>(f1, f2, g1, g2, dL, inv_count,
-                                                             per_image, total);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, scale_fields_vec4, reinterpret_cast<const float4 *>(f1),
+                                  reinterpret_cast<const float4 *>(f2), reinterpret_cast<float4 *>(g1),
+                                  reinterpret_cast<float4 *>(g2), dL, inv_count, per_image / 4,
+                                  total / 4);
+    return cudaLaunchKernelEx(&cfg, scale_fields_scalar, f1, f2, g1, g2, dL, inv_count, per_image,
+                              total);
 }
 
 }  // namespace gbssim

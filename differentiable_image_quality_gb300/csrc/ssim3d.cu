@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     float4 *hy = hx + 2 * IY * HXP;  // kStatsXBytes after hx
     __shared__ double red[NT / 32];
     __shared__ uint64_t bars[NBUF];
+    pdl_trigger();
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -401,6 +402,8 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes + kChainBytes);  // [2][IY][HXP]
     float4 *uy = ux + 2 * IY * HXP;                                       // [2][TY][TX]
     __shared__ uint64_t bars[NBUF];
+    pdl_trigger();
+    pdl_wait();  // the derivative field of the statistics kernel ahead on the stream
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -667,11 +670,18 @@ cudaError_t ssim3d_stats_launch(const Ssim3dArgs &a, bool grad, int blocks, cuda
 
 cudaError_t ssim3d_adjoint_launch(const Ssim3dArgs &a, bool g2, int blocks, cudaStream_t s)
 {
-    if (g2)
-        ssim3d_adjoint_kernel<true><<<blocks, GA::NT, ssim3d_adjoint_smem(), s>>>(a);
-    else
-        ssim3d_adjoint_kernel<false><<<blocks, GA::NT, ssim3d_adjoint_smem(), s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(GA::NT);
+    cfg.dynamicSmemBytes = ssim3d_adjoint_smem();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (g2) return cudaLaunchKernelEx(&cfg, ssim3d_adjoint_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, ssim3d_adjoint_kernel<false>, a);
 }
 
 }  // namespace gbssim
