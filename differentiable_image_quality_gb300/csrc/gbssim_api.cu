@@ -677,7 +677,7 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
         a.images = N;
         a.blocks_per_image = int(p.blocks / N);
         a.count = double(C) * double(ho) * double(wo);
-        const cudaError_t e = ssim2d_components_launch(a, int(p.blocks), s);
+        const cudaError_t e = ssim2d_components_launch(a, int(p.blocks), s, o > 0);
         if (e != cudaSuccess) return cuda_fail(e);
         map_pos += 3 * a.map_stride;
     }

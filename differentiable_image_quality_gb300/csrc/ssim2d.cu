@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
     pdl_trigger();
+    pdl_wait();  // launched early (per-octave stage): the kernel ahead wrote our inputs
     const int tid = threadIdx.x;
     const SegWork w = segment_of(a, blockIdx.x);
     const int strip = w.strip, seg = w.seg, plane = w.plane;
@@ -765,10 +766,23 @@ bool encode_rows_map(CUtensorMap &m, const float *ptr, long long planes, int H, 
 }
 
 template <bool GRAD, bool G2, bool COMP = false>
-cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s)
+cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s, bool early = false)
 {
-    ssim2d_stream_kernel<GRAD, G2, COMP><<<blocks, NT, smem_bytes(GRAD, G2), s>>>(a);
-    return cudaGetLastError();
+    if (!early) {
+        ssim2d_stream_kernel<GRAD, G2, COMP><<<blocks, NT, smem_bytes(GRAD, G2), s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem_bytes(GRAD, G2);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ssim2d_stream_kernel<GRAD, G2, COMP>, a);
 }
 
 // Both images one octave down: out(i, j) = mean of the in-range pixels of the
@@ -780,6 +794,8 @@ __global__ void __launch_bounds__(256) downscale2x_kernel(const float *__restric
                                                           float *__restrict__ oy, int H, int W,
                                                           long long rows)
 {
+    pdl_trigger();
+    pdl_wait();  // the previous octave's images (and the kernel ahead) are complete
     const int Hd = (H + 1) >> 1, Wd = (W + 1) >> 1;
     for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
         const long long plane = row / Hd;
@@ -871,9 +887,9 @@ const void *ssim2d_kernel_ptr(bool grad, bool g2)
               : reinterpret_cast<const void *>(ssim2d_stream_kernel<true, false>);
 }
 
-cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s)
+cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s, bool early)
 {
-    return launch_stream<false, false, true>(a, blocks, s);
+    return launch_stream<false, false, true>(a, blocks, s, early);
 }
 
 const void *ssim2d_components_kernel_ptr()
@@ -886,9 +902,17 @@ cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float 
 {
     const long long rows = planes * ((H + 1) / 2);
     const long long cap = (long long)sm_count * 8;
-    const unsigned blocks = unsigned(rows < cap ? rows : cap);
-    downscale2x_kernel<<<blocks, 256, 0, s>>>(x, y, ox, oy, H, W, rows);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(rows < cap ? rows : cap));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, downscale2x_kernel, x, y, ox, oy, H, W, rows);
 }
 
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)

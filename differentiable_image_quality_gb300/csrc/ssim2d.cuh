@@ -66,9 +66,13 @@ cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, c
 // Forward-only kernel in components mode: l, cs and S maps (a.map, a.map_stride
 // apart) and their per-image means a.mean[j * images + n], j = 0 (l), 1 (cs),
 // 2 (S); a.partials holds 3 x a.segments doubles.  Same plan as the forward.
-cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s);
+// early: launch with programmatic stream serialisation (the kernel waits for
+// the kernel ahead on the stream before reading anything).
+cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s,
+                                     bool early);
 const void *ssim2d_components_kernel_ptr();
-// Both images one octave down (2x2 box means, ragged edges over in-range pixels).
+// Both images one octave down (2x2 box means, ragged edges over in-range
+// pixels); launched early, it waits for the kernel ahead on the stream.
 cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
                                long long planes, int H, int W, int sm_count, cudaStream_t s);
 
