@@ -387,7 +387,8 @@ def run_ours(args):
 
     def e2e_pipelined(steps, warmup):
         copied = [torch.cuda.Event() for _ in range(2)]
-        freed = [None, None]
+        freed = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         if world > 1:
@@ -399,7 +400,7 @@ def run_ours(args):
             if k == warmup:
                 t0.record(copy_stream)
             with torch.cuda.stream(copy_stream):
-                if freed[b] is not None:
+                if used[b]:
                     copy_stream.wait_event(freed[b])
                 dx.copy_(hx, non_blocking=True)
                 dy.copy_(hy, non_blocking=True)
@@ -408,8 +409,8 @@ def run_ours(args):
             fwd_call(dx, dy, wl.padding, mean, saved=saved, want_grad2=g2wanted)
             bwd_call(tdl, dx, dy, wl.padding, g1, g2, saved=saved)
             hloss[k].copy_(mean, non_blocking=True)
-            freed[b] = torch.cuda.Event()
             freed[b].record(stream)
+            used[b] = True
         t1.record(stream)
         torch.cuda.synchronize()
         if world > 1:
