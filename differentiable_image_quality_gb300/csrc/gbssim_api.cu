@@ -26,7 +26,7 @@ struct DeviceInfo {
     int sm_count = 0;
     int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
     int occ_comp = 0;          // components mode of the forward
-    int occ3d[2] = {0, 0};     // statistics kernel, adjoint kernel
+    int occ3d[5] = {0, 0, 0, 0, 0};  // 3D: xy; z forward, gradient, + grad2; adjoint
 };
 
 std::mutex g_mutex;
@@ -290,7 +290,8 @@ bool shape2d_ok(int N, int C, int H, int W, int padding)
 
 // ---- 3D
 
-constexpr int kMinZSeg = 12;  // shortest z segment the planner uses
+constexpr int kMinZSeg = 12;      // shortest z segment of the z kernel
+constexpr int kMinSliceSeg = 4;   // ... and of the two slice kernels
 
 bool shape3d_ok(int N, int C, int D, int H, int W, int padding)
 {
@@ -299,36 +300,40 @@ bool shape3d_ok(int N, int C, int D, int H, int W, int padding)
     if (!extent_ok(D, padding) || !extent_ok(H, padding) || !extent_ok(W, padding)) return false;
     if ((long long)N * C > INT_MAX) return false;
     if (D > (1 << 20) || H > (1 << 20) || W > (1 << 20)) return false;
+    if ((long long)H * W > (1LL << 30)) return false;
     return true;
 }
 
 struct Plan3d {
-    int tiles_x = 0, tiles_y = 0, zsegs = 0, zseg_len = 0;
+    int tiles_x = 0, tiles_y = 0, col_blocks = 0, zsegs = 0, zseg_len = 0;
     long long blocks = 0;
 };
 
-// Tiles of 16 x tile_x columns over (rows, cols), z segments over zlen, with the
-// same per-SM cost model as in 2D (a 10-slice warm-up per segment); an SM is
-// taken as saturated at 16 resident warps.
-Plan3d plan3d(long long planes, int zlen, int rows, int cols, int tile_x, int sm_count, int occ)
+// z segments over zlen for per_z blocks of block_warps warps per z range, each
+// segment costing `warm` steps beyond its length.  Per SM: the blocks run in
+// waves of at most occ; a wave of k blocks takes `steps` step times scaled by
+// k / sat when it holds more than sat blocks (an SM is taken as saturated at 16
+// resident warps), else the same as sat blocks would (latency-bound).
+void plan_z(Plan3d &p, long long per_z, int zlen, int warm, int min_seg, int block_warps,
+            int sm_count, int occ)
 {
-    Plan3d p;
-    p.tiles_x = int(ceil_div(cols, tile_x));
-    p.tiles_y = int(ceil_div(rows, kTile3dY));
-    const long long per_z = planes * p.tiles_x * p.tiles_y;
-    const int full = std::max(1, 512 / (kTile3dY * tile_x));  // blocks of 16 warps
+    const int full = std::max(1, 16 / block_warps);
     const int sat = occ < full ? occ : full;
-    const int max_segs = int(ceil_div(zlen, kMinZSeg));
+    const int max_segs = int(ceil_div(zlen, min_seg));
     double best = -1.0;
     long long best_work = 0;
     for (int s = 1; s <= max_segs; ++s) {
         const int len = int(ceil_div(zlen, s));
         const int segs = int(ceil_div(zlen, len));
         const long long blocks = per_z * segs;
-        const long long steps = len + 10;
-        const long long per_sm = ceil_div(blocks, (long long)sm_count);
-        const double eff = double(per_sm < sat ? per_sm : sat) / sat;
-        const double cost = double(per_sm * steps) / eff;
+        const long long steps = len + warm;
+        long long left = ceil_div(blocks, (long long)sm_count);
+        double cost = 0.0;
+        while (left > 0) {
+            const long long k = left < occ ? left : occ;
+            cost += double(steps) * (k > sat ? double(k) / sat : 1.0);
+            left -= k;
+        }
         const long long work = blocks * steps;
         if (best < 0 || cost < best - 1e-9 || (cost <= best + 1e-9 && work < best_work)) {
             best = cost;
@@ -338,23 +343,47 @@ Plan3d plan3d(long long planes, int zlen, int rows, int cols, int tile_x, int sm
             p.blocks = blocks;
         }
     }
+}
+
+// A slice kernel: tiles of 16 x tile_x over (rows, cols), every slice of the
+// volume walked once (a segment's only extra cost is its pipeline fill).
+Plan3d plan_slices(long long planes, int D, int rows, int cols, int tile_x, int sm_count, int occ)
+{
+    Plan3d p;
+    p.tiles_x = int(ceil_div(cols, tile_x));
+    p.tiles_y = int(ceil_div(rows, kTile3dY));
+    plan_z(p, planes * p.tiles_x * p.tiles_y, D, 2, kMinSliceSeg, kTile3dY * tile_x / 32,
+           sm_count, occ);
     return p;
 }
 
+// The z kernel: blocks of kZThreads output columns; zlen = D with gradients
+// (20 slices of warm-up), Do without (10).
+Plan3d plan_columns(long long planes, int zlen, long long columns, bool grad, int sm_count, int occ)
+{
+    Plan3d p;
+    p.col_blocks = int(ceil_div(columns, (long long)kZThreads));
+    plan_z(p, planes * p.col_blocks, zlen, grad ? 20 : 10, kMinZSeg, kZThreads / 32, sm_count, occ);
+    return p;
+}
+
+// Workspace of the 3D calls: the completion counter, the z kernel's partial
+// sums, then the statistics field and the derivative field, float4 per
+// (plane, slice, output column) each, 256-byte aligned.
 struct Layout3d {
-    size_t partials_off, gfield_off, total;
+    size_t t_off, u_off, total;
 };
 
 Layout3d layout3d(int N, int C, int D, int H, int W, int padding)
 {
     const long long planes = (long long)N * C;
-    const int Do = out_extent(D, padding), Ho = out_extent(H, padding), Wo = out_extent(W, padding);
-    const long long maxb = planes * ceil_div(Wo, kStats3dX) * ceil_div(Ho, kTile3dY) *
-                           ceil_div(Do, kMinZSeg);
+    const long long cols = (long long)out_extent(H, padding) * out_extent(W, padding);
+    const long long maxb = planes * ceil_div(cols, (long long)kZThreads) * ceil_div(D, kMinZSeg);
+    const size_t field = size_t(planes) * D * size_t(cols) * sizeof(float4);
     Layout3d l;
-    l.partials_off = kCounterBytes;
-    l.gfield_off = size_t(ceil_div((long long)(kCounterBytes + maxb * sizeof(double)), 256)) * 256;
-    l.total = l.gfield_off + size_t(planes) * Do * Ho * Wo * 4 * sizeof(float);
+    l.t_off = size_t(ceil_div((long long)(kCounterBytes + maxb * sizeof(double)), 256)) * 256;
+    l.u_off = l.t_off + (field + 255) / 256 * 256;
+    l.total = l.u_off + field;
     return l;
 }
 
@@ -705,14 +734,16 @@ static void fill3d(Ssim3dArgs &a, const float *x, const float *y, int N, int C, 
     a.Do = out_extent(D, padding); a.Ho = out_extent(H, padding); a.Wo = out_extent(W, padding);
     a.off = padding == GBSSIM_VALID ? 0 : kRadius;
     a.C = C;
-    // 16-byte staging of the statistics kernel: tile origins (multiples of 16
-    // minus off) on 16-byte boundaries, 16-byte row pitch, aligned volumes
+    // 16-byte staging of the xy kernel: tile origins (multiples of 8 minus off)
+    // on 16-byte boundaries, 16-byte row pitch, aligned volumes
     a.vec16 = (a.off % 4 == 0) && (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     const Layout3d l = layout3d(N, C, D, H, W, padding);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.counter = reinterpret_cast<unsigned *>(ws);
-    a.gfield = reinterpret_cast<float *>(ws + l.gfield_off);
+    a.partials = reinterpret_cast<double *>(ws + kCounterBytes);
+    a.tfield = reinterpret_cast<float4 *>(ws + l.t_off);
+    a.ufield = reinterpret_cast<float4 *>(ws + l.u_off);
     a.inv_count = float(1.0 / (double(C) * a.Do * a.Ho * a.Wo));
     a.count = double(C) * a.Do * a.Ho * a.Wo;
     a.images = N;
@@ -721,7 +752,38 @@ static void fill3d(Ssim3dArgs &a, const float *x, const float *y, int N, int C, 
 
 static void apply_plan(Ssim3dArgs &a, const Plan3d &p)
 {
-    a.tiles_x = p.tiles_x; a.tiles_y = p.tiles_y; a.zsegs = p.zsegs; a.zseg_len = p.zseg_len;
+    a.tiles_x = p.tiles_x; a.tiles_y = p.tiles_y; a.col_blocks = p.col_blocks;
+    a.zsegs = p.zsegs; a.zseg_len = p.zseg_len;
+}
+
+// The passes of one 3D call on stream s: xy, z (mean into `mean` unless null,
+// map unless null; derivatives when grad), then with grad the adjoint kernel
+// writing out1 (and out2 when g2), scaled by dL[n] (1 when null) / count.
+static int run3d(const DeviceInfo *d, Ssim3dArgs &a, int N, float *mean, float *map, bool grad,
+                 bool g2, float *out1, float *out2, const float *dL, cudaStream_t s)
+{
+    const long long planes = (long long)N * a.C;
+    const Plan3d px = plan_slices(planes, a.D, a.Ho, a.Wo, kXy3dX, d->sm_count, d->occ3d[0]);
+    const Plan3d pz = plan_columns(planes, grad ? a.D : a.Do, (long long)a.Ho * a.Wo, grad,
+                                   d->sm_count, d->occ3d[grad ? (g2 ? 3 : 2) : 1]);
+    Plan3d pa;
+    if (grad) pa = plan_slices(planes, a.D, a.H, a.W, kAdj3dX, d->sm_count, d->occ3d[4]);
+    if (px.blocks > INT_MAX || pz.blocks > INT_MAX || pa.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    apply_plan(a, px);
+    cudaError_t e = ssim3d_xy_launch(a, int(px.blocks), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    apply_plan(a, pz);
+    if (!mean) a.partials = nullptr;
+    a.mean = mean;
+    a.map = map;
+    a.blocks_per_image = int(pz.blocks / N);
+    e = ssim3d_z_launch(a, grad, g2, int(pz.blocks), s);
+    if (e != cudaSuccess || !grad) return cuda_fail(e);
+    apply_plan(a, pa);
+    a.out1 = out1;
+    a.out2 = out2;
+    a.dL = dL;
+    return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pa.blocks), s));
 }
 
 int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
@@ -751,22 +813,9 @@ int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
-    if (pa.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    apply_plan(a, pa);
-    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
-    a.mean = out_mean;
-    a.map = out_map_or_null;
-    a.blocks_per_image = int(pa.blocks / N);
-    cudaError_t e = ssim3d_stats_launch(a, grad, int(pa.blocks), s);
-    if (e != cudaSuccess || !grad) return cuda_fail(e);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
-    if (pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    apply_plan(a, pb);
-    a.out1 = saved_or_null;
-    a.out2 = want_grad2 ? saved_or_null + size_t(N) * C * D * H * W : nullptr;
-    a.dL = nullptr;
-    return cuda_fail(ssim3d_adjoint_launch(a, want_grad2 != 0, int(pb.blocks), s));
+    float *f2 = (grad && want_grad2) ? saved_or_null + size_t(N) * C * D * H * W : nullptr;
+    return run3d(d, a, N, out_mean, out_map_or_null, grad, grad && want_grad2, saved_or_null, f2,
+                 nullptr, s);
 }
 
 int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int D,
@@ -816,19 +865,7 @@ int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int
                                              size_t(C) * D * H * W, total, d->sm_count, s));
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
-    if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    apply_plan(a, pa);
-    a.partials = nullptr;
-    a.map = nullptr;
-    cudaError_t e = ssim3d_stats_launch(a, true, int(pa.blocks), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    apply_plan(a, pb);
-    a.out1 = grad_img1;
-    a.out2 = grad_img2_or_null;
-    a.dL = dL;
-    return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pb.blocks), s));
+    return run3d(d, a, N, nullptr, nullptr, true, g2, grad_img1, grad_img2_or_null, dL, s);
 }
 
 
@@ -923,21 +960,7 @@ int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Ssim3dArgs a{};
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
-    const Plan3d pa = plan3d((long long)N * C, a.Do, a.Ho, a.Wo, kStats3dX, d->sm_count, d->occ3d[0]);
-    const Plan3d pb = plan3d((long long)N * C, D, H, W, kAdj3dX, d->sm_count, d->occ3d[1]);
-    if (pa.blocks > INT_MAX || pb.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    apply_plan(a, pa);
-    a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
-    a.mean = out_mean;
-    a.map = out_map_or_null;
-    a.blocks_per_image = int(pa.blocks / N);
-    cudaError_t e = ssim3d_stats_launch(a, true, int(pa.blocks), s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    apply_plan(a, pb);
-    a.out1 = grad_img1;
-    a.out2 = grad_img2_or_null;
-    a.dL = dL;
-    return cuda_fail(ssim3d_adjoint_launch(a, g2, int(pb.blocks), s));
+    return run3d(d, a, N, out_mean, out_map_or_null, true, g2, grad_img1, grad_img2_or_null, dL, s);
 }
 
 }  // extern "C"

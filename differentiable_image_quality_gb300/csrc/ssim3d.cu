@@ -1,27 +1,26 @@
 // 3D SSIM (fused-ssim README, "3D data"): the same statistics and adjoint as in
 // 2D with an 11x11x11 separable window on NCDHW volumes.
 //
-// Following that page's plan -- keep the 2D convolution on XY slices, and do
-// the Z convolution and SSIM per depth row, one depth row per thread --
-// a CTA owns an XY tile of 16 x 8 (statistics) or 16 x 16 (adjoint) columns and
-// walks along Z one slice per step:
-//   XY  the slice's row pass and column pass in shared memory (the slice tile
-//       plus its 10-pixel halo staged by tensor copies -- one thread issues
-//       them, a transaction barrier per buffer tracks them, every wait bounded
-//       -- or by cp.async where the tile does not start on a 16-byte column;
-//       NBUF buffers, a slice's copies issued NBUF - 3 steps before it is
-//       waited for);
-//   Z   each thread keeps, in registers, the partial sums of the ten Z windows
-//       its column has open (a shift register); each new XY-blurred slice
-//       completes one window and advances the others.
-// Two kernels:
-//   stats    statistics -> SSIM (mean, map) and, for gradients, the derivatives
-//            of SSIM with respect to the four shifted moments, one float4 per
-//            output voxel, into the workspace;
-//   adjoint  the same walk over those derivative fields (the blur's adjoint is
-//            the blur with the window mirrored, which for a symmetric window is
-//            the same correlation with the "full" extent), then the chain rule
-//            grad1 = B^T g_mu1 + 2 x B^T g_e + y B^T g_e12 (grad2 likewise).
+// Three passes whose intermediates stay in L2 (at 128^3 the two volumes, the
+// statistics field and the derivative field together take well under its
+// 129 MB), so that each axis's halo is computed once:
+//   xy   per slice, the row pass and column pass of the four shifted statistics
+//        on an XY tile plus its 10-pixel halo in shared memory -> tfield, one
+//        float4 per (slice, output column); the slice tiles are staged by
+//        tensor copies (one thread issues them, a transaction barrier per
+//        buffer tracks them, every wait bounded) or by cp.async where the tile
+//        does not start on a 16-byte column, NBUF slices in flight;
+//   z    one thread per output column walks along Z: the Z window sums as a
+//        shift register of pending sums, SSIM (mean, map) and, for gradients,
+//        the derivatives of SSIM with respect to the four shifted moments,
+//        whose Z adjoint (the same correlation with the "full" extent, the
+//        window being symmetric) runs as a second shift register -> ufield;
+//   adj  per slice, the XY adjoint of those four fields on a tile plus halo
+//        in shared memory, then the chain rule
+//        grad1 = B^T g_mu1 + 2 x' B^T g_e + y' B^T g_e12 (grad2 likewise).
+// The page's own plan keeps the 2D convolution per slice and runs Z per depth
+// row in one kernel; walking Z inside the slice kernels re-runs the XY work of
+// each Z segment's 10-slice warm-up, which these passes avoid.
 // All window sums run on float pairs (fma.rn.f32x2): (mu1, mu2), (es, e12) for
 // the statistics, (g_mu1, g_e), (g_e12, g_mu2) for the adjoint.  Work items of
 // the row passes are numbered row-fastest over odd shared-memory pitches, so
@@ -33,10 +32,9 @@
 namespace gbssim {
 namespace {
 
-// Tile geometry of a 3D kernel: TY x TX columns, one thread per column.  The
-// statistics kernel runs 16 x 8 tiles (128 threads, four blocks per SM), the
-// adjoint kernel 16 x 16 tiles (256 threads, two blocks per SM): measured on
-// the 128^3 volume, each is the faster shape for its kernel.
+// Tile geometry of a slice kernel: TY x TX columns, one thread per column.  The
+// xy kernel runs 16 x 8 tiles (128 threads), the adjoint kernel 16 x 16 tiles
+// (256 threads).
 template <int TX_>
 struct Geo {
     static constexpr int TY = kTile3dY, TX = TX_, NT = TY * TX;
@@ -57,8 +55,8 @@ struct Geo {
     static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
     static_assert((CSTAGE * 4) % 128 == 0, "chain tiles stay 128-byte aligned");
 };
-using GS = Geo<kStats3dX>;  // statistics kernel
-using GA = Geo<kAdj3dX>;    // adjoint kernel
+using GS = Geo<kXy3dX>;   // xy kernel
+using GA = Geo<kAdj3dX>;  // adjoint kernel
 
 constexpr int NBUF = 6;         // staged slices in flight
 constexpr int CBUF = NBUF + 1;  // adjoint: chain-rule pixel tiles in flight
@@ -67,6 +65,7 @@ constexpr unsigned kAdjTx =
     unsigned(GA::IY * GA::GXP * sizeof(float4) + 2 * GA::CSTAGE * sizeof(float));
 constexpr long long kWaitCycles = 1LL << 31;   // staging wait limit (about a second)
 constexpr long long kDrainCycles = 1LL << 27;  // after a failed wait: copies still in flight
+constexpr int kZPrefetch = 8;                  // z kernel: slices loaded ahead
 
 __device__ unsigned g_staging3d_status;  // bit 0: a staging wait ran out of time
 
@@ -77,6 +76,9 @@ constexpr size_t kAdjInBytes = size_t(NBUF) * GA::GSTAGE * sizeof(float4);
 constexpr size_t kChainBytes = size_t(2) * CBUF * GA::CSTAGE * sizeof(float);
 constexpr size_t kAdjXBytes = size_t(2) * GA::IY * GA::HXP * sizeof(float4);
 constexpr size_t kAdjYBytes = size_t(2) * GA::TY * GA::TX * sizeof(float4);
+
+size_t xy_smem() { return 128 + kStatsInBytes + kStatsXBytes + kStatsYBytes; }
+size_t adjoint_smem() { return 128 + kAdjInBytes + kChainBytes + kAdjXBytes + kAdjYBytes; }
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ float2 splat(float w) { return make_float2(w, w); }
@@ -120,13 +122,13 @@ __device__ __forceinline__ void taps3(const float4 *src, int stride, float2 (&oa
     }
 }
 
-// The Z pass as a shift register of pending window sums.  P[j] holds, after
+// A Z pass as a shift register of pending window sums.  P[j] holds, after
 // slice s, the part of the window that completes at slice s + j + 1 contributed
 // by slices <= s.  Slice s with value h completes the window of P[0] (h is its
 // newest slice, weight w_10) and shifts the rest:
 //   out = P[0] + w_10 h,  P[j] = P[j + 1] + w_{9-j} h (j < 9),  P[9] = w_0 h.
 // Every register index is fixed, so no step dispatches on s % 11, and the 11
-// updates are independent.  Same sum as the symmetric ring, other order.
+// updates are independent.
 __device__ __forceinline__ float2 zshift2(float2 (&P)[kTaps - 1], float2 h)
 {
     const float2 out = __ffma2_rn(splat(tap(10)), h, P[0]);
@@ -145,7 +147,24 @@ __device__ __forceinline__ float zshift1(float (&P)[kTaps - 1], float h)
     return out;
 }
 
-// ------------------------------------------------------------------ kernel A
+// The same register fed a zero (a slice past the end of the domain).
+__device__ __forceinline__ float2 zshift2_zero(float2 (&P)[kTaps - 1])
+{
+    const float2 out = P[0];
+#pragma unroll
+    for (int j = 0; j < kTaps - 2; ++j) P[j] = P[j + 1];
+    P[kTaps - 2] = f2(0.f, 0.f);
+    return out;
+}
+
+__device__ __forceinline__ float zshift1_zero(float (&P)[kTaps - 1])
+{
+    const float out = P[0];
+#pragma unroll
+    for (int j = 0; j < kTaps - 2; ++j) P[j] = P[j + 1];
+    P[kTaps - 2] = 0.f;
+    return out;
+}
 
 // Slices j < waited have been waited for, j < issued copied: after a failed
 // wait, let the copies still in flight land (bounded), then record the failure.
@@ -159,8 +178,15 @@ __device__ __forceinline__ void drain_failed(uint64_t *bars, int waited, int iss
     atomicOr(&g_staging3d_status, 1u);
 }
 
-template <bool GRAD>
-__global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_constant__ Ssim3dArgs a)
+__device__ __forceinline__ float4 nan4()
+{
+    const float q = __int_as_float(0x7fc00000);
+    return make_float4(q, q, q, q);
+}
+
+// ------------------------------------------------------------------ xy kernel
+
+__global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_constant__ Ssim3dArgs a)
 {
     constexpr int NT = GS::NT, TY = GS::TY, TX = GS::TX, IY = GS::IY, IX = GS::IX,
                   IXP = GS::IXP, HXP = GS::HXP, KX = GS::KX, NXI = GS::NXI, KY = GS::KY,
@@ -171,7 +197,6 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     float *ys = xs + NBUF * XSTAGE;
     float4 *hx = reinterpret_cast<float4 *>(smem_raw + kStatsInBytes);
     float4 *hy = hx + 2 * IY * HXP;  // kStatsXBytes after hx
-    __shared__ double red[NT / 32];
     __shared__ uint64_t bars[NBUF];
     pdl_trigger();
 
@@ -185,15 +210,15 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     const float *__restrict__ xp = a.x + size_t(plane) * vol;
     const float *__restrict__ yp = a.y + size_t(plane) * vol;
 
-    const int y0 = tile_y * TY, x0 = tile_x * TX;       // statistic coordinates
+    const int y0 = tile_y * TY, x0 = tile_x * TX;  // output-domain coordinates
     const int z0 = zseg * a.zseg_len;
-    const int z1 = min(z0 + a.zseg_len, a.Do);
-    const int iy0 = y0 - a.off, ix0 = x0 - a.off, iz0 = z0 - a.off;
-    const int nz = z1 - z0 + 10;                        // input slices walked
+    const int z1 = min(z0 + a.zseg_len, a.D);
+    const int iy0 = y0 - a.off, ix0 = x0 - a.off;
+    const int nz = z1 - z0;  // slices walked
 
     auto load_slice = [&](int s) {
         const int buf = s % NBUF;
-        const int Z = iz0 + s;
+        const int Z = z0 + s;
         if (a.tma) {
             if (tid == 0) {
                 mbar_arrive_expect_tx(&bars[buf], kStatsTx + a.tx_extra);
@@ -202,7 +227,6 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
             }
             return;
         }
-        const bool zin = (Z >= 0) && (Z < a.D);
         if (a.vec16) {
             // the tile origin ix0 is a multiple of 4 and W % 4 == 0: 16-byte chunks,
             // each entirely inside or outside the volume
@@ -210,7 +234,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
             for (int e = tid; e < IY * NCH; e += NT) {
                 const int r = e / NCH, ch = e - r * NCH;
                 const int Y = iy0 + r, X = ix0 + 4 * ch;
-                const bool inb = zin && (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
+                const bool inb = (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
                 const size_t gi = inb ? (size_t(Z) * a.H + Y) * a.W + X : 0;
                 const int si = buf * XSTAGE + r * IXP + 4 * ch;
                 cp_async16(xs + si, xp + gi, inb);
@@ -221,7 +245,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
         for (int e = tid; e < IY * IX; e += NT) {
             const int r = e / IX, c = e - r * IX;
             const int Y = iy0 + r, X = ix0 + c;
-            const bool inb = zin && (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
+            const bool inb = (Y >= 0) && (Y < a.H) && (X >= 0) && (X < a.W);
             const size_t gi = inb ? (size_t(Z) * a.H + Y) * a.W + X : 0;
             const int si = buf * XSTAGE + r * IXP + c;
             cp_async4(xs + si, xp + gi, inb);
@@ -281,48 +305,25 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     const int ty = tid / TX, tx = tid - ty * TX;
     const int py = y0 + ty, px = x0 + tx;
     const bool col_ok = (py < a.Ho) && (px < a.Wo);
-    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, e12)
-#pragma unroll
-    for (int k = 0; k < kTaps - 1; ++k) PA[k] = PB[k] = f2(0.f, 0.f);
-    float ssum = 0.0f;
+    float4 *__restrict__ tcol =
+        a.tfield + (size_t(plane) * a.D + z0) * a.Ho * a.Wo + size_t(col_ok ? py : 0) * a.Wo + px;
+    const size_t tstride = size_t(a.Ho) * a.Wo;
 
-    // Z step: this column's XY-blurred value of slice s completes the window of
-    // output slice s - 10.
-    auto z_step = [&](int s) {
-        const float4 h = hy[((s & 1) * TY + ty) * TX + tx];
-        const float2 M = zshift2(PA, lo(h)), E = zshift2(PB, hi(h));
-        const int p = z0 + s - 10;
-        if (s >= 10 && p < z1 && col_ok) {
-            const Moments mo{M.x, M.y, E.x, E.y};
-            float S;
-            const size_t oi = ((size_t(plane) * a.Do + p) * a.Ho + py) * a.Wo + px;
-            if (GRAD) {
-                MomentGrads gg;
-                S = ssim_and_grads<true>(mo, true, gg);
-                reinterpret_cast<float4 *>(a.gfield)[oi] = make_float4(gg.g_m1, gg.g_e, gg.g_e12, gg.g_m2);
-            } else {
-                S = ssim_value(mo);
-            }
-            ssum += S;
-            if (a.map) a.map[oi] = S;
-        }
-    };
-
-    // Pipeline: step s runs the Z pass of slice s, the column pass of slice
-    // s + 1 and the row pass of slice s + 2, then one barrier.  The row and
-    // column results are double-buffered by slice parity, so each buffer a step
-    // writes was last read in the step before.  Slices 0 .. NBUF-1 are in flight
-    // from the start (one commit group each); slice s + NBUF is issued at step s
-    // into the buffer the row pass of slice s released two steps earlier.
-    // Tensor staging waits on slice j's barrier (use j / NBUF of buffer
-    // j % NBUF); a wait that runs out stops the walk (the block's mean is NaN).
+    // Pipeline: step s stores slice s, runs the column pass of slice s + 1 and
+    // the row pass of slice s + 2, then one barrier.  The row and column results
+    // are double-buffered by slice parity, so each buffer a step writes was last
+    // read in the step before.  Slices 0 .. NBUF-1 are in flight from the start
+    // (one commit group each); slice s + NBUF is issued at step s into the
+    // buffer the row pass of slice s released two steps earlier.  Tensor
+    // staging waits on slice j's barrier (use j / NBUF of buffer j % NBUF); a
+    // wait that runs out stops the walk and the block's slices come out NaN.
     auto landed = [&](int j) {
         return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
     };
     if (a.tma) {
         if (tid == 0) {
 #pragma unroll
-            for (int b = 0; b < NBUF; ++b) mbar_init(&bars[b], 1);
+            for (int b2 = 0; b2 < NBUF; ++b2) mbar_init(&bars[b2], 1);
             mbar_init_fence();
         }
         __syncthreads();
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
-        z_step(s);
+        if (col_ok) tcol[s * tstride] = hy[((s & 1) * TY + ty) * TX + tx];
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
         for (int i = tid; i < ny + nx; i += NT) {
@@ -377,16 +378,143 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_stats_kernel(const __grid_co
         waited = min(nz, s + 4);
     }
     cp_async_wait<0>();
-    if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
-
-    if (a.partials) {
-        const double tot = block_sum<NT>(ssum, red);
-        if (tid == 0) a.partials[blockIdx.x] = failed ? __longlong_as_double(0x7ff8000000000000LL) : tot;
-        finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
+    if (failed) {
+        if (a.tma && tid == 0) drain_failed(bars, waited, issued);
+        if (col_ok)
+            for (int s = 0; s < nz; ++s) tcol[s * tstride] = nan4();
     }
 }
 
-// ------------------------------------------------------------------ kernel B
+// ------------------------------------------------------------------- z kernel
+
+// Shifted statistics of a slice of padding (same padding, outside the volume):
+// every pixel is 0, i.e. -kShift after the shift, blurred by the XY window.
+__device__ __forceinline__ float4 pad_stats()
+{
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) t += tap(k);
+    const float s2 = t * t;
+    return make_float4(-kShift * s2, -kShift * s2, 2.0f * kShift * kShift * s2, kShift * kShift * s2);
+}
+
+// One thread per output column (Ho x Wo, flattened) and z segment.  With
+// gradients the segments cut the volume's slices [0, D): segment [z0, z1) of
+// ufield needs the derivatives of output slices z0 + off - 10 .. z1 + off - 1,
+// hence the statistics of slices z0 - 10 .. z1 + 9 (20 slices of warm-up).
+// Without, they cut the output slices [0, Do) (10 slices of warm-up).  SSIM
+// of output slice p counts (mean, map) in the segment that holds p.
+template <bool GRAD, bool G2>
+__global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_constant__ Ssim3dArgs a)
+{
+    __shared__ double red[kZThreads / 32];
+    pdl_trigger();
+    int b = blockIdx.x;
+    const int cb = b % a.col_blocks; b /= a.col_blocks;
+    const int zseg = b % a.zsegs;
+    const int plane = b / a.zsegs;
+    const int cols = a.Ho * a.Wo;
+    const int c = cb * kZThreads + threadIdx.x;
+    const bool col_ok = c < cols;
+    const size_t base = size_t(plane) * a.D * cols + (col_ok ? c : 0);
+    const float4 *__restrict__ tcol = a.tfield + base;
+    float4 *__restrict__ ucol = a.ufield + base;
+    const int off = a.off;
+    const int z0 = zseg * a.zseg_len;
+    const int z1 = min(z0 + a.zseg_len, GRAD ? a.D : a.Do);
+    const int plo = GRAD ? max(z0 + off - 10, 0) : z0;       // output slices computed
+    const int phi = GRAD ? min(z1 + off, a.Do) : z1;
+    const int t0 = plo - off;                                  // first statistics slice
+    const int nfeed = phi - plo + 10;
+    const float4 kpad = pad_stats();
+    const size_t ostride = size_t(cols);
+    float *mapc = a.map ? a.map + (size_t(plane) * a.Do) * cols + (col_ok ? c : 0) : nullptr;
+
+    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, e12)
+    float2 QA[kTaps - 1], QB[kTaps - 1];  // adjoint: of (g_m1, g_e), (g_e12, g_m2)
+    float QC[kTaps - 1];                  // adjoint: of g_e12 alone without grad_img2
+#pragma unroll
+    for (int k = 0; k < kTaps - 1; ++k) {
+        PA[k] = PB[k] = QA[k] = QB[k] = f2(0.f, 0.f);
+        QC[k] = 0.f;
+    }
+    float ssum = 0.f;
+
+    auto emit = [&](int p, const float2 &vA, const float2 &vB, float v12) {
+        const int z = p - off;  // ufield slice completed by output slice p
+        if (z >= z0 && col_ok)
+            ucol[size_t(z) * ostride] = G2 ? make_float4(vA.x, vA.y, vB.x, vB.y)
+                                           : make_float4(vA.x, vA.y, v12, 0.f);
+    };
+
+    // feed i: statistics slice t0 + i; from i = 10 on it completes output slice
+    // plo + i - 10
+    auto step = [&](int i, const float4 &h) {
+        const float2 M = zshift2(PA, lo(h)), E = zshift2(PB, hi(h));
+        if (i < 10) return;
+        const int p = plo + i - 10;
+        const Moments mo{M.x, M.y, E.x, E.y};
+        const bool own = GRAD ? (p >= z0 && p < z1) : true;
+        float S;
+        if (GRAD) {
+            MomentGrads g;
+            S = ssim_and_grads<G2>(mo, true, g);
+            const float2 vA = zshift2(QA, f2(g.g_m1, g.g_e));
+            float2 vB = f2(0.f, 0.f);
+            float v12 = 0.f;
+            if (G2) vB = zshift2(QB, f2(g.g_e12, g.g_m2));
+            else v12 = zshift1(QC, g.g_e12);
+            emit(p, vA, vB, v12);
+        } else {
+            S = ssim_value(mo);
+        }
+        if (own && col_ok) {
+            ssum += S;
+            if (mapc) mapc[size_t(p) * ostride] = S;
+        }
+    };
+
+    auto fetch = [&](int i) -> float4 {
+        const int t = t0 + i;
+        if (i >= nfeed || !col_ok) return make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < 0 || t >= a.D) return kpad;
+        return __ldcg(tcol + size_t(t) * ostride);
+    };
+
+    pdl_wait();  // tfield of the xy kernel ahead on the stream
+    // rolling prefetch: slot j holds feed i0 + j; it is refilled with feed
+    // i0 + j + kZPrefetch as soon as it is taken
+    float4 q[kZPrefetch];
+#pragma unroll
+    for (int j = 0; j < kZPrefetch; ++j) q[j] = fetch(j);
+    for (int i0 = 0; i0 < nfeed; i0 += kZPrefetch) {
+#pragma unroll
+        for (int j = 0; j < kZPrefetch; ++j) {
+            const float4 h = q[j];
+            q[j] = fetch(i0 + j + kZPrefetch);
+            if (i0 + j < nfeed) step(i0 + j, h);
+        }
+    }
+    if (GRAD) {
+        // derivative slices past the output domain are zero: flush the rest
+        for (int p = phi; p < z1 + off; ++p) {
+            const float2 vA = zshift2_zero(QA);
+            float2 vB = f2(0.f, 0.f);
+            float v12 = 0.f;
+            if (G2) vB = zshift2_zero(QB);
+            else v12 = zshift1_zero(QC);
+            emit(p, vA, vB, v12);
+        }
+    }
+
+    if (a.partials) {
+        const double tot = block_sum<kZThreads>(ssum, red);
+        if (threadIdx.x == 0) a.partials[blockIdx.x] = tot;
+        finish_means<kZThreads>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
+    }
+}
+
+// ------------------------------------------------------------- adjoint kernel
 
 template <bool G2>
 __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
@@ -403,7 +531,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     float4 *uy = ux + 2 * IY * HXP;                                       // [2][TY][TX]
     __shared__ uint64_t bars[NBUF];
     pdl_trigger();
-    pdl_wait();  // the derivative field of the statistics kernel ahead on the stream
+    pdl_wait();  // ufield of the z kernel ahead on the stream
 
     const int tid = threadIdx.x;
     int b = blockIdx.x;
@@ -414,45 +542,41 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     const int n = plane / a.C;
     const size_t vol = size_t(a.D) * a.H * a.W;
     const size_t plane_off = size_t(plane) * vol;
-    const float4 *__restrict__ gf = reinterpret_cast<const float4 *>(a.gfield) +
-                                    size_t(plane) * a.Do * a.Ho * a.Wo;
+    const float4 *__restrict__ gf = a.ufield + size_t(plane) * a.D * a.Ho * a.Wo;
 
     const int y0 = tile_y * TY, x0 = tile_x * TX;  // gradient (image) coordinates
     const int q0 = zseg * a.zseg_len;
     const int q1 = min(q0 + a.zseg_len, a.D);
     // derivative positions feeding gradient q: q + off - 10 .. q + off per axis
-    const int gy0 = y0 + a.off - 10, gx0 = x0 + a.off - 10, gz0 = q0 + a.off - 10;
-    const int nz = q1 - q0 + 10;
+    const int gy0 = y0 + a.off - 10, gx0 = x0 + a.off - 10;
+    const int nz = q1 - q0;
     const float scale = a.dL ? a.dL[n] * a.inv_count : a.inv_count;
 
-    // derivative slice gz0 + s, and the input pixels of gradient slice
-    // q0 + s - 10 (the chain rule of step s) into chain buffer s % CBUF
+    // derivative slice q0 + s and the input pixels of the same slice into
+    // chain buffer s % CBUF
     auto load_slice = [&](int s) {
         const int buf = s % NBUF;
-        const int P = gz0 + s;
-        const int q = q0 + s - 10;
-        if (a.tma) {
-            // zeros outside the derivative domain and the volume; the chain tile
-            // of a warm-up step (q < q0) is loaded but not used
+        const int q = q0 + s;
+        if (a.tma_adj) {
+            // zeros outside the derivative domain
             if (tid == 0) {
                 mbar_arrive_expect_tx(&bars[buf], kAdjTx + a.tx_extra);
-                tma_load_4d(gs + buf * GSTAGE, &a.tm_g, 4 * gx0, gy0, P, plane, &bars[buf]);
+                tma_load_4d(gs + buf * GSTAGE, &a.tm_g, 4 * gx0, gy0, q, plane, &bars[buf]);
                 tma_load_4d(cbx + (s % CBUF) * CSTAGE, &a.tm_cx, x0, y0, q, plane, &bars[buf]);
                 tma_load_4d(cby + (s % CBUF) * CSTAGE, &a.tm_cy, x0, y0, q, plane, &bars[buf]);
             }
             return;
         }
-        const bool zin = (P >= 0) && (P < a.Do);
         for (int e = tid; e < IY * IX; e += NT) {
             const int r = e / IX, c = e - r * IX;
             const int Y = gy0 + r, X = gx0 + c;
-            const bool inb = zin && (Y >= 0) && (Y < a.Ho) && (X >= 0) && (X < a.Wo);
-            const size_t gi = inb ? (size_t(P) * a.Ho + Y) * a.Wo + X : 0;
+            const bool inb = (Y >= 0) && (Y < a.Ho) && (X >= 0) && (X < a.Wo);
+            const size_t gi = inb ? (size_t(q) * a.Ho + Y) * a.Wo + X : 0;
             cp_async16(gs + buf * GSTAGE + r * GXP + c, gf + gi, inb);
         }
         const int ty = tid / TX, tx = tid - ty * TX;  // one pixel per thread (NT == TY * TX)
         const int qy = y0 + ty, qx = x0 + tx;
-        const bool inb = (q >= q0) && (q < q1) && (qy < a.H) && (qx < a.W);
+        const bool inb = (qy < a.H) && (qx < a.W);
         const size_t gi = inb ? plane_off + (size_t(q) * a.H + qy) * a.W + qx : 0;
         cp_async4(cbx + (s % CBUF) * CSTAGE + tid, a.x + gi, inb);
         cp_async4(cby + (s % CBUF) * CSTAGE + tid, a.y + gi, inb);
@@ -498,42 +622,27 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     const int ty = tid / TX, tx = tid - ty * TX;
     const int qy = y0 + ty, qx = x0 + tx;
     const bool col_ok = (qy < a.H) && (qx < a.W);
-    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (g_m1, g_e), (g_e12, g_mu2)
-    float PC[kTaps - 1];                 // of g_e12 alone without grad_img2
-#pragma unroll
-    for (int k = 0; k < kTaps - 1; ++k) {
-        PA[k] = PB[k] = f2(0.f, 0.f);
-        PC[k] = 0.f;
-    }
+    const size_t gbase = plane_off + size_t(col_ok ? qy : 0) * a.W + qx;
+    const size_t gstride = size_t(a.H) * a.W;
 
-    auto z_step = [&](int s) {
+    // chain rule of slice s: (B^T g_m1, B^T g_e, B^T g_e12, B^T g_m2) at this pixel
+    auto chain_step = [&](int s) {
+        if (!col_ok) return;
         const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
-        const float2 vA = zshift2(PA, lo(h));  // (B^T g_m1, B^T g_e)
-        float2 vB = f2(0.f, 0.f);              // (B^T g_e12, B^T g_m2)
-        float v12 = 0.f;                       // B^T g_e12
-        if (G2) vB = zshift2(PB, hi(h));
-        else v12 = zshift1(PC, h.z);
-        const int q = q0 + s - 10;
-        if (s >= 10 && q < q1 && col_ok) {
-            const size_t gi = plane_off + (size_t(q) * a.H + qy) * a.W + qx;
-            const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
-            const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
-            if (G2) {
-                a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, vB.x, vA.x));
-                a.out2[gi] = scale * fmaf(2.0f * y, vA.y, fmaf(x, vB.x, vB.y));
-            } else {
-                a.out1[gi] = scale * fmaf(2.0f * x, vA.y, fmaf(y, v12, vA.x));
-            }
-        }
+        const size_t gi = gbase + size_t(q0 + s) * gstride;
+        const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
+        const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
+        a.out1[gi] = scale * fmaf(2.0f * x, h.y, fmaf(y, h.z, h.x));
+        if (G2) a.out2[gi] = scale * fmaf(2.0f * y, h.y, fmaf(x, h.z, h.w));
     };
 
-    // The pipeline of the statistics kernel.  Chain buffer (s + NBUF) % CBUF,
-    // filled at step s, held slice s - 1's pixels, read by the Z pass of the
-    // step before.
+    // The pipeline of the xy kernel, with the chain rule in place of the
+    // store.  Chain buffer (s + NBUF) % CBUF, filled at step s, held slice
+    // s - 1's pixels, read by the chain rule of the step before.
     auto landed = [&](int j) {
         return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
     };
-    if (a.tma) {
+    if (a.tma_adj) {
         if (tid == 0) {
 #pragma unroll
             for (int b2 = 0; b2 < NBUF; ++b2) mbar_init(&bars[b2], 1);
@@ -551,7 +660,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
         cp_async_commit();
     }
     bool ok = true;
-    if (a.tma) ok = landed(0) && landed(1);
+    if (a.tma_adj) ok = landed(0) && landed(1);
     else cp_async_wait<NBUF - 2>();  // slices 0 and 1
     bool failed = __syncthreads_or(!ok);
     if (!failed) {
@@ -563,14 +672,14 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
             if (i < NYI) y_item(0, i);
             else x_item(1, i - NYI);
         }
-        if (a.tma) ok = landed(2);
+        if (a.tma_adj) ok = landed(2);
         else cp_async_wait<NBUF - 3>();  // slice 2
         failed = __syncthreads_or(!ok);
         if (!failed) waited = min(nz, 3);
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
-        z_step(s);
+        chain_step(s);
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
         for (int i = tid; i < ny + nx; i += NT) {
@@ -582,7 +691,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
             ++issued;
         }
         cp_async_commit();
-        if (a.tma) ok = landed(s + 3);
+        if (a.tma_adj) ok = landed(s + 3);
         else cp_async_wait<NBUF - 3>();  // slice s + 3 (and its chain tile) landed
         if (__syncthreads_or(!ok)) {
             failed = true;
@@ -591,7 +700,15 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
         waited = min(nz, s + 4);
     }
     cp_async_wait<0>();
-    if (failed && a.tma && tid == 0) drain_failed(bars, waited, issued);
+    if (failed) {
+        if (a.tma_adj && tid == 0) drain_failed(bars, waited, issued);
+        if (col_ok)
+            for (int s = 0; s < nz; ++s) {
+                const size_t gi = gbase + size_t(q0 + s) * gstride;
+                a.out1[gi] = nan4().x;
+                if (G2) a.out2[gi] = nan4().x;
+            }
+    }
 }
 
 template <typename K>
@@ -603,36 +720,59 @@ cudaError_t prepare(K kernel, int threads, size_t smem, int *occ)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kernel, threads, smem);
 }
 
-}  // namespace
+template <typename K>
+cudaError_t launch_early(K kernel, const Ssim3dArgs &a, int blocks, int threads, size_t smem,
+                         cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
-size_t ssim3d_stats_smem() { return 128 + kStatsInBytes + kStatsXBytes + kStatsYBytes; }
-size_t ssim3d_adjoint_smem() { return 128 + kAdjInBytes + kChainBytes + kAdjXBytes + kAdjYBytes; }
+}  // namespace
 
 void ssim3d_prepare_staging(Ssim3dArgs &a, long long planes)
 {
     const int mode = staging_mode();
-    // vec16: valid padding (tile columns start on 16-byte boundaries),
-    // W % 4 == 0 and 16-byte aligned volumes
-    bool ok = mode != 1 && a.vec16 && a.off == 0 && planes < (1LL << 31);
-    if (ok) {
-        const unsigned long long W = a.W, H = a.H, D = a.D, P = planes;
-        const unsigned long long dims[4] = {W, H, D, P};
-        const unsigned long long st[3] = {W * 4, H * W * 4, D * H * W * 4};
-        const unsigned bx[4] = {GS::IXP, GS::IY, 1, 1}, bc[4] = {GA::TX, GA::TY, 1, 1};
-        ok = encode_tiled_f32(a.tm_x, a.x, 4, dims, st, bx) &&
-             encode_tiled_f32(a.tm_y, a.y, 4, dims, st, bx) &&
-             encode_tiled_f32(a.tm_cx, a.x, 4, dims, st, bc) &&
-             encode_tiled_f32(a.tm_cy, a.y, 4, dims, st, bc);
+    // the volumes as [planes][D][H][W]: W % 4 == 0, 16-byte aligned
+    const bool aligned = mode != 1 && a.W % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(a.y) % 16 == 0 && planes < (1LL << 31);
+    const unsigned long long W = a.W, H = a.H, D = a.D, P = planes;
+    const unsigned long long dims[4] = {W, H, D, P};
+    const unsigned long long st[3] = {W * 4, H * W * 4, D * H * W * 4};
+    // xy kernel: tiles start at x0 - off, on 16-byte columns in valid padding
+    bool xy = aligned && a.off == 0;
+    if (xy) {
+        const unsigned bx[4] = {GS::IXP, GS::IY, 1, 1};
+        xy = encode_tiled_f32(a.tm_x, a.x, 4, dims, st, bx) &&
+             encode_tiled_f32(a.tm_y, a.y, 4, dims, st, bx);
     }
-    if (ok) {
-        const unsigned long long Wo = a.Wo, Ho = a.Ho, Do = a.Do, P = planes;
-        const unsigned long long dims[4] = {4 * Wo, Ho, Do, P};
-        const unsigned long long st[3] = {Wo * 16, Ho * Wo * 16, Do * Ho * Wo * 16};
+    // adjoint kernel: chain tiles at multiples of 16 columns, derivative tiles
+    // at 4 (x0 + off - 10) floats of float4 rows (16-byte columns in both paddings)
+    bool adj = aligned && a.ufield;
+    if (adj) {
+        const unsigned bc[4] = {GA::TX, GA::TY, 1, 1};
+        adj = encode_tiled_f32(a.tm_cx, a.x, 4, dims, st, bc) &&
+              encode_tiled_f32(a.tm_cy, a.y, 4, dims, st, bc);
+    }
+    if (adj) {
+        const unsigned long long Wo = a.Wo, Ho = a.Ho;
+        const unsigned long long gdims[4] = {4 * Wo, Ho, D, P};
+        const unsigned long long gst[3] = {Wo * 16, Ho * Wo * 16, D * Ho * Wo * 16};
         const unsigned bg[4] = {4 * GA::GXP, GA::IY, 1, 1};
-        ok = a.gfield && encode_tiled_f32(a.tm_g, a.gfield, 4, dims, st, bg);
+        adj = encode_tiled_f32(a.tm_g, a.ufield, 4, gdims, gst, bg);
     }
-    a.tma = ok ? 1 : 0;
-    a.tx_extra = (ok && mode == 2) ? 16u : 0u;
+    a.tma = xy ? 1 : 0;
+    a.tma_adj = adj ? 1 : 0;
+    a.tx_extra = ((xy || adj) && mode == 2) ? 16u : 0u;
 }
 
 cudaError_t ssim3d_staging_status(unsigned *flags, bool clear)
@@ -645,43 +785,42 @@ cudaError_t ssim3d_staging_status(unsigned *flags, bool clear)
     return e;
 }
 
-cudaError_t ssim3d_prepare(int occ[2])
+cudaError_t ssim3d_prepare(int occ[5])
 {
-    int o[4] = {0, 0, 0, 0};
+    int o[6] = {0, 0, 0, 0, 0, 0};
     cudaError_t e;
-    const size_t ss = ssim3d_stats_smem(), sa = ssim3d_adjoint_smem();
-    if ((e = prepare(ssim3d_stats_kernel<false>, GS::NT, ss, &o[0])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_stats_kernel<true>, GS::NT, ss, &o[1])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_adjoint_kernel<false>, GA::NT, sa, &o[2])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_adjoint_kernel<true>, GA::NT, sa, &o[3])) != cudaSuccess) return e;
-    occ[0] = o[0] < o[1] ? o[0] : o[1];
-    occ[1] = o[2] < o[3] ? o[2] : o[3];
-    return (occ[0] < 1 || occ[1] < 1) ? cudaErrorInvalidConfiguration : cudaSuccess;
+    if ((e = prepare(ssim3d_xy_kernel, GS::NT, xy_smem(), &o[0])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<false, false>, kZThreads, 0, &o[1])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<true, false>, kZThreads, 0, &o[2])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<true, true>, kZThreads, 0, &o[3])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_adjoint_kernel<false>, GA::NT, adjoint_smem(), &o[4])) != cudaSuccess)
+        return e;
+    if ((e = prepare(ssim3d_adjoint_kernel<true>, GA::NT, adjoint_smem(), &o[5])) != cudaSuccess)
+        return e;
+    for (int i = 0; i < 4; ++i) occ[i] = o[i];
+    occ[4] = o[4] < o[5] ? o[4] : o[5];
+    for (int i = 0; i < 5; ++i)
+        if (occ[i] < 1) return cudaErrorInvalidConfiguration;
+    return cudaSuccess;
 }
 
-cudaError_t ssim3d_stats_launch(const Ssim3dArgs &a, bool grad, int blocks, cudaStream_t s)
+cudaError_t ssim3d_xy_launch(const Ssim3dArgs &a, int blocks, cudaStream_t s)
 {
-    if (grad)
-        ssim3d_stats_kernel<true><<<blocks, GS::NT, ssim3d_stats_smem(), s>>>(a);
-    else
-        ssim3d_stats_kernel<false><<<blocks, GS::NT, ssim3d_stats_smem(), s>>>(a);
+    ssim3d_xy_kernel<<<blocks, GS::NT, xy_smem(), s>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t ssim3d_z_launch(const Ssim3dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)
+{
+    if (!grad) return launch_early(ssim3d_z_kernel<false, false>, a, blocks, kZThreads, 0, s);
+    if (g2) return launch_early(ssim3d_z_kernel<true, true>, a, blocks, kZThreads, 0, s);
+    return launch_early(ssim3d_z_kernel<true, false>, a, blocks, kZThreads, 0, s);
 }
 
 cudaError_t ssim3d_adjoint_launch(const Ssim3dArgs &a, bool g2, int blocks, cudaStream_t s)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(blocks));
-    cfg.blockDim = dim3(GA::NT);
-    cfg.dynamicSmemBytes = ssim3d_adjoint_smem();
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (g2) return cudaLaunchKernelEx(&cfg, ssim3d_adjoint_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, ssim3d_adjoint_kernel<false>, a);
+    if (g2) return launch_early(ssim3d_adjoint_kernel<true>, a, blocks, GA::NT, adjoint_smem(), s);
+    return launch_early(ssim3d_adjoint_kernel<false>, a, blocks, GA::NT, adjoint_smem(), s);
 }
 
 }  // namespace gbssim
