@@ -48,10 +48,10 @@ PROFILE3D = os.path.join(ROOT, "profiles", "ssim3d_volume128_valid.md")
 GRAD_FMA_PER_PIXEL = 44 + 44 + 33 + 33  # row + column passes of 4 statistics, of 3 adjoint maps
 GRAD_OTHER_PER_PIXEL = 5 + 30 + 3       # shifted products, SSIM and derivatives, chain rule
 GRAD_FLOPS_PER_PIXEL = 2 * GRAD_FMA_PER_PIXEL + GRAD_OTHER_PER_PIXEL
-# 3D (statistics and adjoint kernels together): three 11-tap passes of four
+# 3D (the three kernels of the training forward together): three 11-tap passes of four
 # statistics and of three adjoint maps, plus the same per-voxel work.
 GRAD3D_FLOPS_PER_VOXEL = 2 * (3 * 44 + 3 * 33) + GRAD_OTHER_PER_PIXEL
-KERNEL3D_NAME = "ssim3d_stats_kernel<true> + ssim3d_adjoint_kernel<false>"
+KERNEL3D_NAME = "ssim3d_xy_kernel + ssim3d_z_kernel<true,false> + ssim3d_adjoint_kernel<false>"
 
 
 def parse():

@@ -200,9 +200,10 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
 /* fused-ssim README, "3D data": the same statistics with an 11x11x11 window on
  * NCDHW volumes.  Arguments mean what they mean in 2D, with D added; both
  * paddings apply to all three axes (valid needs D, H, W >= 11).
- * The 3D calls keep the per-voxel derivatives of SSIM between their two
- * kernels in the workspace, so ssim3d_bwd takes one too (it is only used when
- * saved_or_null is NULL). */
+ * The 3D calls keep two fields between their three kernels in the workspace:
+ * the XY-blurred statistics of every slice and the Z-blurred derivatives of
+ * SSIM, one float4 per (slice, output column) each; so ssim3d_bwd takes a
+ * workspace too (it is only used when saved_or_null is NULL). */
 
 /* Workspace bytes of ssim3d_fwd / ssim3d_bwd (0 for an invalid shape).  Same
  * zero-fill rule as gbssim_workspace_bytes. */

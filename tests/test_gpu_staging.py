@@ -1,10 +1,12 @@
 """The two ways the 2D and 3D kernels stage their inputs, and the bounded
 staging wait.
 
-On 16-byte aligned images with W % 4 == 0 (3D: and valid padding) the
-kernels stage rows and slice tiles with tensor copies (one thread per block
-issues them; a transaction barrier tracks them); otherwise, or when the
-staging hook asks for it, every thread issues cp.async copies.  Both must give the oracle's results.  A wait for a tensor copy is
+On 16-byte aligned images with W % 4 == 0 the kernels stage rows and slice
+tiles with tensor copies (one thread per block issues them; a transaction
+barrier tracks them) -- in 3D the XY statistics kernel only in valid padding,
+the adjoint kernel in both (its tiles of the derivative field start at
+negative coordinates in same padding); otherwise, or when the staging hook asks
+for it, every thread issues cp.async copies.  Both must give the oracle's results.  A wait for a tensor copy is
 bounded: when it runs out, the kernel's blocks stop, the device records the
 failure, the affected means come out NaN, and the context stays usable.  The
 hook's mode 2 makes every wait run out by announcing 16 bytes more than the
@@ -98,18 +100,21 @@ def test_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-@pytest.mark.parametrize("shape", [(1, 1, 13, 20, 36), (2, 1, 12, 12, 12)])
-def test_both_3d_staging_paths_match_the_oracle(lib, oracle_mod, shape, mode):
+@pytest.mark.parametrize("shape,padding", [((1, 1, 13, 20, 36), "valid"),
+                                           ((2, 1, 12, 12, 12), "valid"),
+                                           ((1, 1, 13, 20, 36), "same"),
+                                           ((1, 2, 7, 24, 16), "same")])
+def test_both_3d_staging_paths_match_the_oracle(lib, oracle_mod, shape, padding, mode):
     import torch
 
     x, y = uniform_pair(shape, 970 + shape[4], std=0.08)
     dl = np.linspace(-1.0, 0.5, shape[0])
-    ref = _oracle(oracle_mod, x, y, dl, "valid", True, want_map=True)
+    ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
     lib.gbssim_tune_staging(mode)
     try:
         for path in ("saved", "recompute"):
-            got = _run(torch.device("cuda:0"), x, y, dl, "valid", True, path, want_map=True)
-            _assert_parity(got, ref, True, f"3D mode {mode} {shape} {path}")
+            got = _run(torch.device("cuda:0"), x, y, dl, padding, True, path, want_map=True)
+            _assert_parity(got, ref, True, f"3D mode {mode} {shape} {padding} {path}")
     finally:
         lib.gbssim_tune_staging(0)
 
