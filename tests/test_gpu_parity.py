@@ -162,6 +162,10 @@ SMALL_3D = [
     ((1, 1, 40, 36, 70), "valid", 6),   # ragged tiles (16 x 32) in both directions
     ((1, 1, 1, 1, 1), "same", 7),
     ((1, 1, 3, 40, 2), "same", 8),
+    ((1, 1, 150, 11, 12), "valid", 9),  # one output column block, many z segments
+    ((1, 1, 90, 2, 3), "same", 10),     # long thin columns, padding slices at both ends
+    ((3, 1, 12, 30, 17), "same", 11),   # several images: per-image means of the z kernel
+    ((1, 1, 25, 140, 12), "valid", 12), # more columns than one z-kernel block
 ]
 
 
