@@ -506,7 +506,8 @@ def run_ours(args):
                    "timing": "CUDA events around each step (forward + backward) on the launching "
                              "stream; value = K steps / sum; fwd_ms, bwd_ms from a second pass "
                              "with an event between them"},
-        "gpu_launches": (2 if not is3d else 3) * args.steps,
+        # per step: the forward kernel(s) (2D: one; 3D: xy, z, adjoint) and the scaling backward
+        "gpu_launches": (2 if not is3d else 4) * args.steps,
         "roofline": {"kernel": KERNEL_NAME if not is3d else KERNEL3D_NAME, "bound": "alu",
                      "achieved": achieved_tflops, "peak": alu_peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved_tflops / alu_peak_tflops,
