@@ -14,7 +14,7 @@ from workloads import uniform_pair
 
 pytestmark = pytest.mark.gpu
 
-N_2D, N_3D = 14, 6
+N_2D, N_3D = 14, 12
 
 
 def _draw_2d(i):
