@@ -268,19 +268,11 @@ __device__ __forceinline__ double block_sum(float v, double *scratch /* NT/32 do
     return t;
 }
 
-// Grid-wide finish of per-image means.  Every block calls this once, with its
-// partial sums already written (and fenced) at partials[k * stride + slot],
-// k < K.  The last block to arrive reduces, for every quantity k and image n,
-// the blocks_per_image consecutive partials of that image -- one warp per
-// (k, n), its lanes striding the partials, then a fixed shuffle tree: a fixed
-// order, so the result is deterministic -- and writes
-// mean[k * images + n] = sum / count.  It then resets the counter to zero for
-// the next call.  The (k, n) reductions run in parallel: each costs one round
-// of L2 loads.
-template <int NT, int K>
-__device__ __forceinline__ void finish_means_k(double *partials, int stride, unsigned *counter,
-                                               float *mean, int images, int blocks_per_image,
-                                               double count)
+// Last-block ticket of a grid-wide finish: every block calls this once, after
+// its partial sums are written; true (in every thread) in the block that
+// arrives last, whose view of all partials is then complete.
+template <int NT>
+__device__ __forceinline__ bool finish_ticket(unsigned *counter)
 {
     __shared__ bool last;
     if (threadIdx.x == 0) {
@@ -289,8 +281,20 @@ __device__ __forceinline__ void finish_means_k(double *partials, int stride, uns
         last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
-    if (!last) return;
-    __threadfence();
+    if (last) __threadfence();
+    return last;
+}
+
+// Per-image means from block partial sums: for every quantity k < K and image
+// n, the blocks_per_image consecutive partials at partials[k * stride +
+// n * blocks_per_image ...] -- one warp per (k, n), its lanes striding the
+// partials, then a fixed shuffle tree: a fixed order, so the result is
+// deterministic -- give mean[k * images + n] = sum / count.  The (k, n)
+// reductions run in parallel: each costs one round of L2 loads.
+template <int NT, int K>
+__device__ __forceinline__ void reduce_means_k(const double *partials, int stride, float *mean,
+                                               int images, int blocks_per_image, double count)
+{
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int q = warp; q < K * images; q += NT / 32) {
         const int k = q / images, n = q - k * images;
@@ -301,6 +305,17 @@ __device__ __forceinline__ void finish_means_k(double *partials, int stride, uns
         for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
         if (lane == 0) mean[k * images + n] = static_cast<float>(s / count);
     }
+}
+
+// Grid-wide finish of per-image means: the last block to arrive reduces them
+// (reduce_means_k) and resets the counter to zero for the next call.
+template <int NT, int K>
+__device__ __forceinline__ void finish_means_k(double *partials, int stride, unsigned *counter,
+                                               float *mean, int images, int blocks_per_image,
+                                               double count)
+{
+    if (!finish_ticket<NT>(counter)) return;
+    reduce_means_k<NT, K>(partials, stride, mean, images, blocks_per_image, count);
     if (threadIdx.x == 0) *counter = 0u;
 }
 

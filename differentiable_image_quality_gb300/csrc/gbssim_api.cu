@@ -26,6 +26,7 @@ struct DeviceInfo {
     int sm_count = 0;
     int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
     int occ_comp = 0;          // components mode of the forward
+    int occ_multi = 0;         // ... several octaves in one launch
     int occ3d[5] = {0, 0, 0, 0, 0};  // 3D: xy; z forward, gradient, + grad2; adjoint
 };
 
@@ -61,15 +62,18 @@ int device_info(DeviceInfo **out)
             if (e != cudaSuccess) return cuda_fail(e);
             if (d.occ2d[i] < 1) return cuda_fail(cudaErrorInvalidConfiguration);
         }
-        {
-            const void *k = ssim2d_components_kernel_ptr();
+        for (int multi = 0; multi < 2; ++multi) {
+            const void *k = multi ? ssim2d_components_multi_kernel_ptr()
+                                  : ssim2d_components_kernel_ptr();
             const size_t smem = ssim2d_smem_bytes(false, false);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  int(smem));
             if (e != cudaSuccess) return cuda_fail(e);
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_comp, k, kThreads2d, smem);
+            int occ = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads2d, smem);
             if (e != cudaSuccess) return cuda_fail(e);
-            if (d.occ_comp < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+            if (occ < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+            (multi ? d.occ_multi : d.occ_comp) = occ;
         }
         const cudaError_t e3 = ssim3d_prepare(d.occ3d);
         if (e3 != cudaSuccess) return cuda_fail(e3);
@@ -221,6 +225,24 @@ Plan2d plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bool grad
         if (cost < best - 1e-9) best_k = k;
     }
     take(best_k);
+    return p;
+}
+
+// A forward-mode plan of about `target` blocks: every strip of every plane cut
+// into the same number of row segments (within the planner's limits).
+Plan2d plan2d_blocks(long long planes, int Ho, int Wo, int off, long long target)
+{
+    Plan2d p;
+    const int S = ssim2d_strips(false, 0, Wo, off);  // forward strips depend on Wo only
+    p.strips = S;
+    const int max_segs = std::max(1, Ho / kMinSegRowsFwd);
+    long long per_plane = target / planes;
+    per_plane = std::max<long long>(S, std::min<long long>(per_plane, (long long)S * max_segs));
+    p.per_plane = int(per_plane);
+    p.base = p.per_plane / S;
+    p.extra = p.per_plane % S;
+    p.blocks = planes * p.per_plane;
+    p.long_blocks = planes * (S - p.extra) * p.base;
     return p;
 }
 
@@ -393,9 +415,9 @@ constexpr int kMaxOctaves = 32;
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// Workspace of ssim_pyramid: the completion counter, 3 x (most blocks of any
-// octave) partial sums, then the downscaled pair of each octave >= 1 (every
-// image 256-byte aligned).
+// Workspace of ssim_pyramid: the completion counter, the partial sums (3 per
+// block of every octave: they are planned into one launch), then the
+// downscaled pair of each octave >= 1 (every image 256-byte aligned).
 struct PyrLayout {
     int octaves = 0;
     int H[kMaxOctaves], W[kMaxOctaves];
@@ -408,7 +430,7 @@ bool pyramid_layout(int N, int C, int H, int W, int padding, int octaves, PyrLay
     if (octaves < 1 || octaves > kMaxOctaves || !shape2d_ok(N, C, H, W, padding)) return false;
     const long long planes = (long long)N * C;
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    long long max_blocks = 0;
+    long long first_blocks = 0, later_blocks = 0;
     int h = H, w = W;
     L.octaves = octaves;
     L.map_floats = 0;
@@ -417,11 +439,12 @@ bool pyramid_layout(int N, int C, int H, int W, int padding, int octaves, PyrLay
         L.H[o] = h;
         L.W[o] = w;
         const int ho = out_extent(h, padding), wo = out_extent(w, padding);
-        max_blocks = std::max(max_blocks, max_blocks2d(planes, h, w, ho, wo, off));
+        (o == 0 ? first_blocks : later_blocks) += max_blocks2d(planes, h, w, ho, wo, off);
         L.map_floats += 3 * size_t(planes) * size_t(ho) * size_t(wo);
         h = (h + 1) / 2;
         w = (w + 1) / 2;
     }
+    const long long max_blocks = first_blocks + later_blocks;  // one launch, every octave
     size_t pos = round256(kCounterBytes + 3 * size_t(max_blocks) * sizeof(double));
     L.x_off[0] = L.y_off[0] = 0;
     for (int o = 1; o < octaves; ++o) {
@@ -671,23 +694,19 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const float *cx = img1, *cy = img2;
-    size_t map_pos = 0;
-    for (int o = 0; o < octaves; ++o) {
+    unsigned *counter = reinterpret_cast<unsigned *>(ws);
+    double *partials = reinterpret_cast<double *>(ws + kCounterBytes);
+    // the components-mode arguments of octave o; its partial sums at `part`
+    auto octave_args = [&](int o, double *part, size_t map_pos, int occ, long long target,
+                           Ssim2dArgs &a, long long &blocks) -> int {
         const int h = L.H[o], w = L.W[o];
-        if (o > 0) {
-            float *ox = reinterpret_cast<float *>(ws + L.x_off[o]);
-            float *oy = reinterpret_cast<float *>(ws + L.y_off[o]);
-            const cudaError_t e =
-                downscale2x_launch(cx, cy, ox, oy, planes, L.H[o - 1], L.W[o - 1], d->sm_count, s);
-            if (e != cudaSuccess) return cuda_fail(e);
-            cx = ox;
-            cy = oy;
-        }
+        const float *cx = o ? reinterpret_cast<const float *>(ws + L.x_off[o]) : img1;
+        const float *cy = o ? reinterpret_cast<const float *>(ws + L.y_off[o]) : img2;
         const int ho = out_extent(h, padding), wo = out_extent(w, padding);
-        const Plan2d p = cached_plan2d(planes, h, w, ho, wo, off, false, d->sm_count, d->occ_comp);
+        const Plan2d p = target > 0 ? plan2d_blocks(planes, ho, wo, off, target)
+                                    : cached_plan2d(planes, h, w, ho, wo, off, false, d->sm_count, occ);
         if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
-        Ssim2dArgs a{};
+        a = Ssim2dArgs{};
         a.x = cx; a.y = cy;
         a.H = h; a.W = w; a.Ho = ho; a.Wo = wo;
         a.off = off;
@@ -700,15 +719,75 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
         a.map = maps_or_null ? maps_or_null + map_pos : nullptr;
         a.map_stride = size_t(planes) * ho * wo;
         a.segments = int(p.blocks);
-        a.counter = reinterpret_cast<unsigned *>(ws);
-        a.partials = reinterpret_cast<double *>(ws + kCounterBytes);
+        a.counter = counter;
+        a.partials = part;
         a.mean = out_means + size_t(o) * 3 * N;
         a.images = N;
         a.blocks_per_image = int(p.blocks / N);
         a.count = double(C) * double(ho) * double(wo);
-        const cudaError_t e = ssim2d_components_launch(a, int(p.blocks), s, o > 0);
-        if (e != cudaSuccess) return cuda_fail(e);
-        map_pos += 3 * a.map_stride;
+        blocks = p.blocks;
+        return GBSSIM_OK;
+    };
+    cudaError_t e;
+    if (octaves == 1) {
+        Ssim2dArgs a0;
+        long long b0 = 0;
+        if ((rc = octave_args(0, partials, 0, d->occ_comp, 0, a0, b0))) return rc;
+        return cuda_fail(ssim2d_components_launch(a0, int(b0), s, false));
+    }
+    // the downscaled octaves first, up to kChainLevels per launch (each waits
+    // for the kernel ahead before its blocks let the launch behind start)
+    for (int lo = 0; lo + 1 < octaves; lo += kChainLevels) {
+        OctaveChainArgs m{};
+        m.levels = std::min(kChainLevels, octaves - 1 - lo);
+        m.x = lo ? reinterpret_cast<const float *>(ws + L.x_off[lo]) : img1;
+        m.y = lo ? reinterpret_cast<const float *>(ws + L.y_off[lo]) : img2;
+        for (int l = 0; l <= m.levels; ++l) {
+            m.H[l] = L.H[lo + l];
+            m.W[l] = L.W[lo + l];
+            if (l > 0) {
+                m.ox[l - 1] = reinterpret_cast<float *>(ws + L.x_off[lo + l]);
+                m.oy[l - 1] = reinterpret_cast<float *>(ws + L.y_off[lo + l]);
+            }
+        }
+        m.tiles_x = int(ceil_div(L.W[lo], kChainTile * kChainG));
+        m.tiles_y = int(ceil_div(L.H[lo], kChainTile));
+        m.planes = planes;
+        m.wait_first = 1;
+        if ((e = octave_chain_launch(m, s)) != cudaSuccess) return cuda_fail(e);
+    }
+    // then the statistics of every octave, up to kMaxMulti octaves per launch;
+    // a launch's blocks fill the GPU's resident slots once, shared among its
+    // octaves by output pixels, so that its blocks end close together
+    size_t map_pos = 0;
+    for (int o0 = 0; o0 < octaves; o0 += kMaxMulti) {
+        Ssim2dMulti m{};
+        m.count = std::min(kMaxMulti, octaves - o0);
+        m.counter = counter;
+        double *part = partials;
+        long long total = 0;
+        double work = 0.0;
+        for (int k = 0; k < m.count; ++k)
+            work += double(out_extent(L.H[o0 + k], padding)) * out_extent(L.W[o0 + k], padding);
+        for (int k = 0; k < m.count; ++k) {
+            long long blocks = 0;
+            const double share = double(out_extent(L.H[o0 + k], padding)) *
+                                 out_extent(L.W[o0 + k], padding) / work;
+            const long long target =
+                std::max(1LL, (long long)(share * d->sm_count * d->occ_multi + 0.5));
+            if ((rc = octave_args(o0 + k, part, map_pos, d->occ_multi, target, m.oct[k], blocks)))
+                return rc;
+            // octave 0 reads the caller's images: its blocks need not wait for the
+            // octave chain ahead (which itself waited for the work before it)
+            m.oct[k].no_wait = (o0 + k == 0) ? 1 : 0;
+            m.first[k] = int(total);
+            total += blocks;
+            if (total > INT_MAX) return GBSSIM_ESHAPE;
+            part += 3 * blocks;
+            map_pos += 3 * m.oct[k].map_stride;
+        }
+        m.first[m.count] = int(total);
+        if ((e = ssim2d_components_multi_launch(m, s)) != cudaSuccess) return cuda_fail(e);
     }
     return GBSSIM_OK;
 }

@@ -41,6 +41,8 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 
+#include <climits>
+
 #include "common.cuh"
 #include "ssim2d.cuh"
 
@@ -199,9 +201,11 @@ __device__ __forceinline__ SegWork segment_of(const Ssim2dArgs &a, int b)
 template <bool GRAD, bool G2>
 constexpr int min_blocks() { return (GRAD && G2) ? 2 : 3; }
 
-template <bool GRAD, bool G2, bool COMP = false>
-__global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
-    ssim2d_stream_kernel(const __grid_constant__ Ssim2dArgs a)
+// The work of one block (block = its index in the launch's plan of `a`).  With
+// MULTI the block's partial sums are written but the means are left to the
+// caller (one finish for several octaves in one launch).
+template <bool GRAD, bool G2, bool COMP, bool MULTI>
+__device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
 {
     static_assert(!(COMP && GRAD), "components mode is forward only");
     constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
@@ -223,9 +227,11 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     __shared__ uint64_t bars[3];  // tensor staging: buffers 0 and 1, chain-rule pixels
 
     pdl_trigger();
-    pdl_wait();  // launched early (per-octave stage): the kernel ahead wrote our inputs
+    // launched early (per-octave stage): the kernel ahead wrote our inputs,
+    // unless they are the caller's images (no_wait)
+    if (!a.no_wait) pdl_wait();
     const int tid = threadIdx.x;
-    const SegWork w = segment_of(a, blockIdx.x);
+    const SegWork w = segment_of(a, block);
     const int strip = w.strip, seg = w.seg, plane = w.plane;
     const int n = plane / a.C;
     const size_t plane_off = size_t(plane) * size_t(a.H) * size_t(a.W);
@@ -682,14 +688,39 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
                 a.partials[a.segments + w.slot] = failed ? nan : tc;
                 a.partials[2 * a.segments + w.slot] = failed ? nan : ts;
             }
-            finish_means_k<NT, 3>(a.partials, a.segments, a.counter, a.mean, a.images,
-                                  a.blocks_per_image, a.count);
+            if (!MULTI)
+                finish_means_k<NT, 3>(a.partials, a.segments, a.counter, a.mean, a.images,
+                                      a.blocks_per_image, a.count);
         } else {
             const double tot = block_sum<NT>(ssum, red[0]);
             if (tid == 0) a.partials[w.slot] = failed ? nan : tot;
             finish_means<NT>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
         }
     }
+}
+
+template <bool GRAD, bool G2, bool COMP = false>
+__global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
+    ssim2d_stream_kernel(const __grid_constant__ Ssim2dArgs a)
+{
+    stream_body<GRAD, G2, COMP, false>(a, blockIdx.x);
+}
+
+// Components mode for several octaves in one launch: block b belongs to the
+// octave o with first[o] <= b < first[o + 1]; the last block to finish reduces
+// every octave's means.
+__global__ void __launch_bounds__(NT, min_blocks<false, false>())
+    ssim2d_components_multi_kernel(const __grid_constant__ Ssim2dMulti m)
+{
+    int o = 0;
+    while (o + 1 < m.count && int(blockIdx.x) >= m.first[o + 1]) ++o;
+    stream_body<false, false, true, true>(m.oct[o], int(blockIdx.x) - m.first[o]);
+    if (!finish_ticket<NT>(m.counter)) return;
+    for (int k = 0; k < m.count; ++k) {
+        const Ssim2dArgs &q = m.oct[k];
+        reduce_means_k<NT, 3>(q.partials, q.segments, q.mean, q.images, q.blocks_per_image, q.count);
+    }
+    if (threadIdx.x == 0) *m.counter = 0u;
 }
 
 // grad = field * dL[n] / count, elementwise; n = index / per_image.
@@ -785,39 +816,112 @@ cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s, bool 
     return cudaLaunchKernelEx(&cfg, ssim2d_stream_kernel<GRAD, G2, COMP>, a);
 }
 
-// Both images one octave down: out(i, j) = mean of the in-range pixels of the
-// 2x2 block at (2i, 2j); planes of H x W -> Hd x Wd = ceil(H/2) x ceil(W/2).
-// Block b handles output rows b, b + gridDim.x, ... (row = plane * Hd + i).
-__global__ void __launch_bounds__(256) downscale2x_kernel(const float *__restrict__ x,
-                                                          const float *__restrict__ y,
-                                                          float *__restrict__ ox,
-                                                          float *__restrict__ oy, int H, int W,
-                                                          long long rows)
+// Octaves lo + 1 .. lo + levels of both images from octave lo, levels <= 5:
+// out(i, j) = mean of the in-range pixels of the 2x2 block at (2i, 2j) of the
+// octave above (extents ceil(H / 2) x ceil(W / 2)), summed in the order
+// (0,0), (0,1), (1,0), (1,1).  A block owns a kChainTile x kChainTile * kChainG
+// tile of octave lo (rows and columns at multiples of the tile), so the tiles
+// of every lower octave lie inside it: each thread forms kChainG pixels of
+// octave lo + 1 straight from global memory, the later octaves are formed
+// level by level in shared memory.  With wait_first the kernel ahead on the
+// stream wrote octave lo; otherwise octave lo is an input and the kernel ahead
+// (whose work this launch overlaps) is only waited for at the end, so that
+// this launch completes after it.
+__device__ __forceinline__ void quad_sum(const float *p, int W, int r, int c, bool r1, bool c1,
+                                         bool pair, float &s)
 {
+    const float *q = p + size_t(r) * W + c;
+    if (pair) {
+        const float2 a = *reinterpret_cast<const float2 *>(q);
+        s = a.x + a.y;
+        if (r1) {
+            const float2 b = *reinterpret_cast<const float2 *>(q + W);
+            s += b.x;
+            s += b.y;
+        }
+        return;
+    }
+    s = q[0];
+    if (c1) s += q[1];
+    if (r1) {
+        s += q[W];
+        if (c1) s += q[W + 1];
+    }
+}
+
+__global__ void __launch_bounds__(256) octave_chain_kernel(const __grid_constant__ OctaveChainArgs m)
+{
+    constexpr int R1 = kChainTile / 2, C1 = kChainTile * kChainG / 2;  // octave lo + 1 tile
+    __shared__ float buf[2][2][R1][C1 + 1];                            // [ping][image][row][col]
+    // the launch behind may start once every block is past this point, i.e.
+    // after the kernel ahead completed (with wait_first)
+    if (m.wait_first) pdl_wait();
     pdl_trigger();
-    pdl_wait();  // the previous octave's images (and the kernel ahead) are complete
-    const int Hd = (H + 1) >> 1, Wd = (W + 1) >> 1;
-    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-        const long long plane = row / Hd;
-        const int i = int(row - plane * Hd);
-        const int r0 = 2 * i;
-        const bool r1 = r0 + 1 < H;
-        const float *px = x + (plane * H + r0) * W, *py = y + (plane * H + r0) * W;
-        float *qx = ox + row * Wd, *qy = oy + row * Wd;
-        for (int j = threadIdx.x; j < Wd; j += blockDim.x) {
-            const int c0 = 2 * j;
-            const bool c1 = c0 + 1 < W;
-            float sx = px[c0], sy = py[c0];
-            if (c1) { sx += px[c0 + 1]; sy += py[c0 + 1]; }
-            if (r1) {
-                sx += px[W + c0]; sy += py[W + c0];
-                if (c1) { sx += px[W + c0 + 1]; sy += py[W + c0 + 1]; }
+    const int tiles = m.tiles_x * m.tiles_y;
+    const long long plane = blockIdx.x / tiles;
+    const int t = int(blockIdx.x - plane * tiles);
+    const int ty = t / m.tiles_x, tx = t - ty * m.tiles_x;
+    {
+        const int H0 = m.H[0], W0 = m.W[0], H1 = m.H[1], W1 = m.W[1];
+        const float *px = m.x + size_t(plane) * H0 * W0, *py = m.y + size_t(plane) * H0 * W0;
+        const bool even = (W0 % 2 == 0) && ((reinterpret_cast<uintptr_t>(m.x) |
+                                              reinterpret_cast<uintptr_t>(m.y)) % 8 == 0);
+        const int i = threadIdx.x / 16;
+#pragma unroll
+        for (int k = 0; k < kChainG; ++k) {
+            const int j = threadIdx.x % 16 + 16 * k;
+            const int gi = ty * R1 + i, gj = tx * C1 + j;
+            float sx = 0.0f, sy = 0.0f;
+            if (gi < H1 && gj < W1) {
+                const bool r1 = 2 * gi + 1 < H0, c1 = 2 * gj + 1 < W0;
+                const bool pair = even && c1;
+                quad_sum(px, W0, 2 * gi, 2 * gj, r1, c1, pair, sx);
+                quad_sum(py, W0, 2 * gi, 2 * gj, r1, c1, pair, sy);
+                const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
+                sx *= inv;
+                sy *= inv;
+                const size_t gidx = (size_t(plane) * H1 + gi) * W1 + gj;
+                m.ox[0][gidx] = sx;
+                m.oy[0][gidx] = sy;
             }
-            const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
-            qx[j] = sx * inv;
-            qy[j] = sy * inv;
+            buf[0][0][i][j] = sx;
+            buf[0][1][i][j] = sy;
         }
     }
+    __syncthreads();
+    int cur = 0;
+    for (int l = 2; l <= m.levels; ++l) {
+        const int nr = R1 >> (l - 1), nc = C1 >> (l - 1);  // tile extent at level l
+        const int Hp = m.H[l - 1], Wp = m.W[l - 1], Hl = m.H[l], Wl = m.W[l];
+        float *ox = m.ox[l - 1], *oy = m.oy[l - 1];
+        for (int e = threadIdx.x; e < nr * nc; e += blockDim.x) {
+            const int i = e / nc, j = e - i * nc;
+            const int gi = ty * nr + i, gj = tx * nc + j;
+            float sx = 0.0f, sy = 0.0f;
+            if (gi < Hl && gj < Wl) {
+                const int r0 = 2 * i, c0 = 2 * j;
+                const bool r1 = 2 * gi + 1 < Hp, c1 = 2 * gj + 1 < Wp;
+                sx = buf[cur][0][r0][c0];
+                sy = buf[cur][1][r0][c0];
+                if (c1) { sx += buf[cur][0][r0][c0 + 1]; sy += buf[cur][1][r0][c0 + 1]; }
+                if (r1) {
+                    sx += buf[cur][0][r0 + 1][c0]; sy += buf[cur][1][r0 + 1][c0];
+                    if (c1) { sx += buf[cur][0][r0 + 1][c0 + 1]; sy += buf[cur][1][r0 + 1][c0 + 1]; }
+                }
+                const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
+                sx *= inv;
+                sy *= inv;
+                const size_t gidx = (size_t(plane) * Hl + gi) * Wl + gj;
+                ox[gidx] = sx;
+                oy[gidx] = sy;
+            }
+            buf[cur ^ 1][0][i][j] = sx;
+            buf[cur ^ 1][1][i][j] = sy;
+        }
+        __syncthreads();
+        cur ^= 1;
+    }
+    pdl_wait();
 }
 
 }  // namespace
@@ -897,13 +1001,12 @@ const void *ssim2d_components_kernel_ptr()
     return reinterpret_cast<const void *>(ssim2d_stream_kernel<false, false, true>);
 }
 
-cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
-                               long long planes, int H, int W, int sm_count, cudaStream_t s)
+cudaError_t octave_chain_launch(const OctaveChainArgs &m, cudaStream_t s)
 {
-    const long long rows = planes * ((H + 1) / 2);
-    const long long cap = (long long)sm_count * 8;
+    const long long blocks = m.planes * m.tiles_x * m.tiles_y;
+    if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(rows < cap ? rows : cap));
+    cfg.gridDim = dim3(unsigned(blocks));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -912,7 +1015,27 @@ cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, downscale2x_kernel, x, y, ox, oy, H, W, rows);
+    return cudaLaunchKernelEx(&cfg, octave_chain_kernel, m);
+}
+
+cudaError_t ssim2d_components_multi_launch(const Ssim2dMulti &m, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(m.first[m.count]));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem_bytes(false, false);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ssim2d_components_multi_kernel, m);
+}
+
+const void *ssim2d_components_multi_kernel_ptr()
+{
+    return reinterpret_cast<const void *>(ssim2d_components_multi_kernel);
 }
 
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)

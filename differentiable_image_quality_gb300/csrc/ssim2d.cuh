@@ -28,6 +28,7 @@ struct Ssim2dArgs {
     // blocks per plane; long_blocks = planes * (strips - seg_extra) * seg_base
     int strips, rows, per_plane, seg_base, seg_extra, long_blocks;
     int vec16;       // 1: W % 4 == 0 and x, y 16-byte aligned (16-byte staging)
+    int no_wait;     // 1: x, y are inputs that the kernel ahead did not write (no wait for it)
     // gradient mode: fields written here (grad of mean[n] * dL[n]); out2 may be null
     float *out1, *out2;
     const float *dL;  // [N] or null (then dL = 1)
@@ -71,10 +72,36 @@ cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, c
 cudaError_t ssim2d_components_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s,
                                      bool early);
 const void *ssim2d_components_kernel_ptr();
-// Both images one octave down (2x2 box means, ragged edges over in-range
-// pixels); launched early, it waits for the kernel ahead on the stream.
-cudaError_t downscale2x_launch(const float *x, const float *y, float *ox, float *oy,
-                               long long planes, int H, int W, int sm_count, cudaStream_t s);
+// Several octaves of the per-octave stage in one components-mode launch
+// (launched early; every block waits for the kernel ahead first).  Octave o
+// owns blocks first[o] .. first[o + 1] - 1 of the grid, each with its own
+// partial-sum area (oct[o].partials, 3 x oct[o].segments); the launch's last
+// block reduces all their means and resets *counter.
+constexpr int kMaxMulti = 8;
+struct Ssim2dMulti {
+    Ssim2dArgs oct[kMaxMulti];
+    int first[kMaxMulti + 1];
+    int count;
+    unsigned *counter;
+};
+cudaError_t ssim2d_components_multi_launch(const Ssim2dMulti &m, cudaStream_t s);
+const void *ssim2d_components_multi_kernel_ptr();
+
+// Octaves lo + 1 .. lo + levels (levels <= kChainLevels) of both images from
+// octave lo in one launch: 2x2 box means, ragged edges over in-range pixels.
+// Launched early; with wait_first the kernel ahead wrote octave lo, otherwise
+// the launch runs beside the kernel ahead and waits for it only at its end.
+constexpr int kChainLevels = 5;
+constexpr int kChainTile = 1 << kChainLevels;  // octave-lo tile of a block: kChainTile rows,
+constexpr int kChainG = 4;                      // kChainTile * kChainG columns
+struct OctaveChainArgs {
+    const float *x, *y;                                // octave lo, [planes][H[0]][W[0]]
+    float *ox[kChainLevels], *oy[kChainLevels];        // octaves lo + 1 .. lo + levels
+    int H[kChainLevels + 1], W[kChainLevels + 1];      // extents of octaves lo .. lo + levels
+    int levels, tiles_x, tiles_y, wait_first;          // tiles over octave lo
+    long long planes;
+};
+cudaError_t octave_chain_launch(const OctaveChainArgs &m, cudaStream_t s);
 
 // g = f * dL[i / per_image] * inv_count for one or two fields (f2/g2 may be null).
 cudaError_t scale_fields_launch(const float *f1, const float *f2, float *g1, float *g2,
