@@ -64,6 +64,9 @@ CASES = [
     ((2, 1, 90, 263), "valid", 4, 5),
     ((1, 1, 1, 1), "same", 2, 6),
     ((3, 1, 11, 11), "valid", 1, 7),
+    ((1, 2, 100, 140), "same", 7, 8),    # two octave-chain launches (5 + 1 octaves)
+    ((1, 1, 300, 517), "same", 10, 9),   # two chain launches (5 + 4), two octave launches (8 + 2)
+    ((2, 1, 70, 33), "same", 6, 10),     # octave tiles wider than the image
 ]
 
 
