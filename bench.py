@@ -199,11 +199,22 @@ def cpu_baseline(name: str, unit: str, target_s: float = 4.0):
     rows, (x, y, dl), _ = size_oracle_band(oracle, name, target_s)
     times = [time_oracle_step(oracle, x, y, dl, wl.padding, wl.want_grad2) for _ in range(3)]
     t = statistics.median(times)
+    cores = oracle.num_threads()
+    # the same on one thread, on a band of about a second
+    rows1 = max(11, int(rows * min(1.0, 1.0 / max(t * cores, 1e-6))))
+    x1, y1, dl1 = oracle_band(name, rows1)
+    oracle.set_num_threads(1)
+    try:
+        t1 = time_oracle_step(oracle, x1, y1, dl1, wl.padding, wl.want_grad2)
+    finally:
+        oracle.set_num_threads(cores)
     what = "rows" if wl.ndim == 2 else "slices"
-    return {"value": units(x.shape) / t, "unit": unit, "cores": oracle.num_threads(),
+    return {"value": units(x.shape) / t, "unit": unit, "cores": cores,
             "kind": "oracle",
             "sample": f"{what} 0..{rows} of the {'x'.join(map(str, wl.shape))} pair ({wl.padding}), "
-                      f"mean + gradients, median of 3 ({t:.2f} s each)"}
+                      f"mean + gradients, median of 3 ({t:.2f} s each)",
+            "value_1_thread": units(x1.shape) / t1,
+            "sample_1_thread": f"{what} 0..{x1.shape[2]}, one run ({t1:.2f} s)"}
 
 
 def run_reference(args):

@@ -118,6 +118,11 @@ def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (independent outputs only)."""
+    _load().oracle_set_num_threads(int(n))
+
+
 def gauss_window() -> np.ndarray:
     w = np.zeros(11, dtype=np.float64)
     _load().oracle_gauss_window(_ptr(w))
