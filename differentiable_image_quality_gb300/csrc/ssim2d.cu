@@ -827,26 +827,45 @@ cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s, bool 
 // stream wrote octave lo; otherwise octave lo is an input and the kernel ahead
 // (whose work this launch overlaps) is only waited for at the end, so that
 // this launch completes after it.
-__device__ __forceinline__ void quad_sum(const float *p, int W, int r, int c, bool r1, bool c1,
-                                         bool pair, float &s)
+// The (up to) four pixels of a 2x2 block of one image: q[0], q[1] of row r
+// and q[2], q[3] of row r + 1; only in-range ones are loaded.
+struct Quad {
+    float v[4];
+};
+
+__device__ __forceinline__ Quad load_quad(const float *__restrict__ p, int W, int r, int c, bool r1,
+                                          bool c1, bool pair)
 {
-    const float *q = p + size_t(r) * W + c;
+    Quad q{{0.f, 0.f, 0.f, 0.f}};
+    const float *a = p + size_t(r) * W + c;
     if (pair) {
-        const float2 a = *reinterpret_cast<const float2 *>(q);
-        s = a.x + a.y;
+        const float2 u = __ldg(reinterpret_cast<const float2 *>(a));
+        q.v[0] = u.x; q.v[1] = u.y;
         if (r1) {
-            const float2 b = *reinterpret_cast<const float2 *>(q + W);
-            s += b.x;
-            s += b.y;
+            const float2 w = __ldg(reinterpret_cast<const float2 *>(a + W));
+            q.v[2] = w.x; q.v[3] = w.y;
         }
-        return;
+        return q;
     }
-    s = q[0];
-    if (c1) s += q[1];
+    q.v[0] = __ldg(a);
+    if (c1) q.v[1] = __ldg(a + 1);
     if (r1) {
-        s += q[W];
-        if (c1) s += q[W + 1];
+        q.v[2] = __ldg(a + W);
+        if (c1) q.v[3] = __ldg(a + W + 1);
     }
+    return q;
+}
+
+// Sum in the order (0,0), (0,1), (1,0), (1,1) of the in-range pixels.
+__device__ __forceinline__ float quad_sum(const Quad &q, bool r1, bool c1)
+{
+    float s = q.v[0];
+    if (c1) s += q.v[1];
+    if (r1) {
+        s += q.v[2];
+        if (c1) s += q.v[3];
+    }
+    return s;
 }
 
 __global__ void __launch_bounds__(256) octave_chain_kernel(const __grid_constant__ OctaveChainArgs m)
@@ -863,23 +882,31 @@ __global__ void __launch_bounds__(256) octave_chain_kernel(const __grid_constant
     const int ty = t / m.tiles_x, tx = t - ty * m.tiles_x;
     {
         const int H0 = m.H[0], W0 = m.W[0], H1 = m.H[1], W1 = m.W[1];
-        const float *px = m.x + size_t(plane) * H0 * W0, *py = m.y + size_t(plane) * H0 * W0;
+        const float *__restrict__ px = m.x + size_t(plane) * H0 * W0;
+        const float *__restrict__ py = m.y + size_t(plane) * H0 * W0;
         const bool even = (W0 % 2 == 0) && ((reinterpret_cast<uintptr_t>(m.x) |
                                               reinterpret_cast<uintptr_t>(m.y)) % 8 == 0);
-        const int i = threadIdx.x / 16;
+        const int i = threadIdx.x / 16, gi = ty * R1 + i;
+        // every load of the thread first, then the sums and stores
+        Quad qx[kChainG], qy[kChainG];
+#pragma unroll
+        for (int k = 0; k < kChainG; ++k) {
+            const int gj = tx * C1 + threadIdx.x % 16 + 16 * k;
+            const bool in = (gi < H1) && (gj < W1);
+            const bool r1 = 2 * gi + 1 < H0, c1 = 2 * gj + 1 < W0;
+            qx[k] = in ? load_quad(px, W0, 2 * gi, 2 * gj, r1, c1, even && c1) : Quad{{0.f, 0.f, 0.f, 0.f}};
+            qy[k] = in ? load_quad(py, W0, 2 * gi, 2 * gj, r1, c1, even && c1) : Quad{{0.f, 0.f, 0.f, 0.f}};
+        }
 #pragma unroll
         for (int k = 0; k < kChainG; ++k) {
             const int j = threadIdx.x % 16 + 16 * k;
-            const int gi = ty * R1 + i, gj = tx * C1 + j;
+            const int gj = tx * C1 + j;
             float sx = 0.0f, sy = 0.0f;
             if (gi < H1 && gj < W1) {
                 const bool r1 = 2 * gi + 1 < H0, c1 = 2 * gj + 1 < W0;
-                const bool pair = even && c1;
-                quad_sum(px, W0, 2 * gi, 2 * gj, r1, c1, pair, sx);
-                quad_sum(py, W0, 2 * gi, 2 * gj, r1, c1, pair, sy);
                 const float inv = (r1 && c1) ? 0.25f : ((r1 || c1) ? 0.5f : 1.0f);
-                sx *= inv;
-                sy *= inv;
+                sx = quad_sum(qx[k], r1, c1) * inv;
+                sy = quad_sum(qy[k], r1, c1) * inv;
                 const size_t gidx = (size_t(plane) * H1 + gi) * W1 + gj;
                 m.ox[0][gidx] = sx;
                 m.oy[0][gidx] = sy;
