@@ -44,7 +44,9 @@ PROFILE3D = os.path.join(ROOT, "profiles", "ssim3d_volume128_valid.md")
 
 # Algorithmic float32 operations of the gradient-mode kernel per input pixel
 # (fused forward statistics, SSIM derivatives, adjoint and chain rule), counting
-# an FMA as 2 flops; derivation in DESIGN.md ("Roofline of each kernel").
+# an FMA as 2 flops: an 11-tap row pass and column pass of the four shifted
+# statistics (44 + 44 FMA) and of the three adjoint maps (33 + 33 FMA), plus
+# the shifted products (5), SSIM and its derivatives (30) and the chain rule (3).
 GRAD_FMA_PER_PIXEL = 44 + 44 + 33 + 33  # row + column passes of 4 statistics, of 3 adjoint maps
 GRAD_OTHER_PER_PIXEL = 5 + 30 + 3       # shifted products, SSIM and derivatives, chain rule
 GRAD_FLOPS_PER_PIXEL = 2 * GRAD_FMA_PER_PIXEL + GRAD_OTHER_PER_PIXEL
