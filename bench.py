@@ -389,12 +389,16 @@ def run_ours(args):
     # per-image means) back; two input buffers let the copy of step k + 1 run
     # on a copy stream while step k computes.  The serial form, which also
     # reads the gradients back, is reported beside it.
-    hx = torch.from_numpy(x).pin_memory()
-    hy = torch.from_numpy(y).pin_memory()
+    # the pair as one pinned host buffer and one device buffer per slot: one
+    # copy per step (img1 and img2 are its two halves)
+    hxy = torch.empty((2,) + tuple(x.shape), dtype=torch.float32).pin_memory()
+    hxy[0].copy_(torch.from_numpy(x))
+    hxy[1].copy_(torch.from_numpy(y))
     hg1 = torch.empty(x.shape, dtype=torch.float32).pin_memory()
     hg2 = torch.empty(x.shape, dtype=torch.float32).pin_memory() if g2wanted else None
     hm = torch.empty(N, dtype=torch.float32).pin_memory()
-    dbuf = [(torch.empty_like(tx), torch.empty_like(ty)) for _ in range(2)]
+    dxy = [torch.empty((2,) + tuple(x.shape), dtype=torch.float32, device=dev) for _ in range(2)]
+    dbuf = [(d[0], d[1]) for d in dxy]
     copy_stream = torch.cuda.Stream(dev)
     hloss = torch.empty((args.steps + max(3, args.warmup), N), dtype=torch.float32).pin_memory()
 
@@ -407,21 +411,22 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        losses = [hloss[k] for k in range(warmup + steps)]
+        on_copy = torch.cuda.stream(copy_stream)
         for k in range(warmup + steps):
             b = k % 2
             dx, dy = dbuf[b]
             if k == warmup:
                 t0.record(copy_stream)
-            with torch.cuda.stream(copy_stream):
+            with on_copy:
                 if used[b]:
                     copy_stream.wait_event(freed[b])
-                dx.copy_(hx, non_blocking=True)
-                dy.copy_(hy, non_blocking=True)
+                dxy[b].copy_(hxy, non_blocking=True)
                 copied[b].record(copy_stream)
             stream.wait_event(copied[b])
             fwd_call(dx, dy, wl.padding, mean, saved=saved, want_grad2=g2wanted)
             bwd_call(tdl, dx, dy, wl.padding, g1, g2, saved=saved)
-            hloss[k].copy_(mean, non_blocking=True)
+            losses[k].copy_(mean, non_blocking=True)
             freed[b].record(stream)
             used[b] = True
         t1.record(stream)
@@ -435,8 +440,7 @@ def run_ours(args):
 
     def e2e_serial_step():
         dx, dy = dbuf[0]
-        dx.copy_(hx, non_blocking=True)
-        dy.copy_(hy, non_blocking=True)
+        dxy[0].copy_(hxy, non_blocking=True)
         fwd_call(dx, dy, wl.padding, mean, saved=saved, want_grad2=g2wanted)
         bwd_call(tdl, dx, dy, wl.padding, g1, g2, saved=saved)
         hg1.copy_(g1, non_blocking=True)
