@@ -138,3 +138,29 @@ def test_3d_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
     ref = _oracle(oracle_mod, x, y, dl, "valid", False)
     _assert_parity(got, ref, False, "3D after a staging timeout")
     assert _status(lib) == 0
+
+
+def test_pyramid_staging_wait_runs_out_and_the_context_survives(lib, oracle_mod):
+    """The per-octave stage's one launch for all octaves takes the same failure
+    path: every octave's means come out NaN, then the same call recovers."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+
+    dev = torch.device("cuda:0")
+    assert _status(lib) == 0, "an earlier call recorded a staging timeout"
+    x, y = uniform_pair((1, 2, 64, 64), 992, std=0.08)
+    tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+    lib.gbssim_tune_staging(2)
+    try:
+        stalled, _ = pkg.ssim_pyramid(tx, ty, "valid", 2)
+        torch.cuda.synchronize()
+    finally:
+        lib.gbssim_tune_staging(0)
+    assert _status(lib) & STAGING_TIMEOUT
+    assert np.all(np.isnan(stalled.cpu().numpy()))
+    assert _status(lib) == 0
+    means, _ = pkg.ssim_pyramid(tx, ty, "valid", 2)
+    ref = oracle_mod.ssim2d_pyramid(x, y, "valid", 2)
+    assert np.max(np.abs(means.cpu().numpy() - ref)) <= 1e-5
+    assert _status(lib) == 0
