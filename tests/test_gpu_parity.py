@@ -356,3 +356,33 @@ def test_single_call_forward_backward(dev, oracle_mod, name):
         got["g2"] = g2.cpu().numpy()
     ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2, want_map=True)
     _assert_parity(got, ref, wl.want_grad2, f"single call {name}")
+
+
+@pytest.mark.parametrize("path", ["saved", "recompute"])
+@pytest.mark.parametrize("ndim", [2, 3])
+def test_nan_propagates_within_its_reach(dev, oracle_mod, path, ndim):
+    """A NaN pixel of one image makes that image's mean NaN and the gradient NaN
+    within 20 pixels of it (window, then adjoint); every other image and every
+    pixel out of that reach keep the oracle's values."""
+    shape = (2, 1, 44, 46) if ndim == 2 else (2, 1, 24, 24, 48)
+    x, y = uniform_pair(shape, 4242 + ndim, std=0.08)
+    dl = np.array([-1.0, 0.5])
+    ref = _oracle(oracle_mod, x, y, dl, "valid", False)  # clean reference
+    c = tuple(s // 2 for s in shape[2:])
+    x = x.copy()
+    x[(0, 0) + c] = np.nan
+    got = _run(dev, x, y, dl, "valid", False, path)
+    assert np.isnan(got["mean"][0])
+    assert abs(got["mean"][1] - ref["mean"][1]) <= MEAN_TOL
+    g = got["g1"]
+    # image 1: unaffected
+    err = np.max(np.abs(g[1] - ref["g1"][1])) / np.max(np.abs(ref["g1"][1]))
+    assert err <= GRAD_RTOL
+    # image 0: NaN inside the reach, the oracle's values (of the clean pair) far from it
+    idx = np.indices(shape[2:])
+    dist = np.max(np.abs(idx - np.array(c).reshape((-1,) + (1,) * len(c))), axis=0)
+    assert np.isnan(g[0, 0][dist <= 10]).all()
+    far = dist > 20
+    assert far.any() and np.isfinite(g[0, 0][far]).all()
+    scale = np.max(np.abs(ref["g1"][0]))
+    assert np.max(np.abs(g[0, 0][far] - ref["g1"][0, 0][far])) / scale <= GRAD_RTOL
