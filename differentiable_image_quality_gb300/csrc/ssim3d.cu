@@ -403,8 +403,10 @@ __device__ __forceinline__ float4 pad_stats()
 // ufield needs the derivatives of output slices z0 + off - 10 .. z1 + off - 1,
 // hence the statistics of slices z0 - 10 .. z1 + 9 (20 slices of warm-up).
 // Without, they cut the output slices [0, Do) (10 slices of warm-up).  SSIM
-// of output slice p counts (mean, map) in the segment that holds p.
-template <bool GRAD, bool G2>
+// of output slice p counts (mean, map) in the segment that holds p.  SAME:
+// same padding (slices outside the volume enter as padding statistics); in
+// valid padding every slice read lies inside the volume.
+template <bool GRAD, bool G2, bool SAME>
 __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_constant__ Ssim3dArgs a)
 {
     __shared__ double red[kZThreads / 32];
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
     const size_t base = size_t(plane) * a.D * cols + (col_ok ? c : 0);
     const float4 *__restrict__ tcol = a.tfield + base;
     float4 *__restrict__ ucol = a.ufield + base;
-    const int off = a.off;
+    constexpr int off = SAME ? kRadius : 0;
     const int z0 = zseg * a.zseg_len;
     const int z1 = min(z0 + a.zseg_len, GRAD ? a.D : a.Do);
     const int plo = GRAD ? max(z0 + off - 10, 0) : z0;       // output slices computed
@@ -474,11 +476,16 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
         }
     };
 
+    // valid padding reads only slices inside the volume
+    const float4 *tnext = tcol + size_t(SAME ? 0 : t0) * ostride;
     auto fetch = [&](int i) -> float4 {
-        const int t = t0 + i;
         if (i >= nfeed || !col_ok) return make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < 0 || t >= a.D) return kpad;
-        return __ldcg(tcol + size_t(t) * ostride);
+        if (SAME) {
+            const int t = t0 + i;
+            if (t < 0 || t >= a.D) return kpad;
+            return __ldcg(tcol + size_t(t) * ostride);
+        }
+        return __ldcg(tnext + size_t(i) * ostride);
     };
 
     pdl_wait();  // tfield of the xy kernel ahead on the stream
@@ -790,9 +797,9 @@ cudaError_t ssim3d_prepare(int occ[5])
     int o[6] = {0, 0, 0, 0, 0, 0};
     cudaError_t e;
     if ((e = prepare(ssim3d_xy_kernel, GS::NT, xy_smem(), &o[0])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_z_kernel<false, false>, kZThreads, 0, &o[1])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_z_kernel<true, false>, kZThreads, 0, &o[2])) != cudaSuccess) return e;
-    if ((e = prepare(ssim3d_z_kernel<true, true>, kZThreads, 0, &o[3])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<false, false, true>, kZThreads, 0, &o[1])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<true, false, true>, kZThreads, 0, &o[2])) != cudaSuccess) return e;
+    if ((e = prepare(ssim3d_z_kernel<true, true, true>, kZThreads, 0, &o[3])) != cudaSuccess) return e;
     if ((e = prepare(ssim3d_adjoint_kernel<false>, GA::NT, adjoint_smem(), &o[4])) != cudaSuccess)
         return e;
     if ((e = prepare(ssim3d_adjoint_kernel<true>, GA::NT, adjoint_smem(), &o[5])) != cudaSuccess)
@@ -812,9 +819,14 @@ cudaError_t ssim3d_xy_launch(const Ssim3dArgs &a, int blocks, cudaStream_t s)
 
 cudaError_t ssim3d_z_launch(const Ssim3dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)
 {
-    if (!grad) return launch_early(ssim3d_z_kernel<false, false>, a, blocks, kZThreads, 0, s);
-    if (g2) return launch_early(ssim3d_z_kernel<true, true>, a, blocks, kZThreads, 0, s);
-    return launch_early(ssim3d_z_kernel<true, false>, a, blocks, kZThreads, 0, s);
+    if (a.off) {
+        if (!grad) return launch_early(ssim3d_z_kernel<false, false, true>, a, blocks, kZThreads, 0, s);
+        if (g2) return launch_early(ssim3d_z_kernel<true, true, true>, a, blocks, kZThreads, 0, s);
+        return launch_early(ssim3d_z_kernel<true, false, true>, a, blocks, kZThreads, 0, s);
+    }
+    if (!grad) return launch_early(ssim3d_z_kernel<false, false, false>, a, blocks, kZThreads, 0, s);
+    if (g2) return launch_early(ssim3d_z_kernel<true, true, false>, a, blocks, kZThreads, 0, s);
+    return launch_early(ssim3d_z_kernel<true, false, false>, a, blocks, kZThreads, 0, s);
 }
 
 cudaError_t ssim3d_adjoint_launch(const Ssim3dArgs &a, bool g2, int blocks, cudaStream_t s)
