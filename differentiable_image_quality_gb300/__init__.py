@@ -16,7 +16,11 @@ SSIM over the batch (a scalar), or the per-image means with per_image=True.
 Both images may require gradients; training code uses ``loss = 1 - fused_ssim(...)``.
 With train=True and a gradient required, the forward also produces the
 gradient fields of the per-image means, so the backward is one scaling pass;
-train=False is the inference mode (and a later backward recomputes).
+train=False is the inference mode (and a later backward recomputes).  The
+choice is per call: a grad-enabled forward that no backward will follow (a
+validation loss under autograd) should pass train=False, which skips the
+gradient work the stored path does inside the forward.  Calls on different
+CUDA streams may run concurrently: each stream gets its own scratch buffer.
 
 The thin wrappers ssim_fwd / ssim_bwd / ssim3d_fwd / ssim3d_bwd expose the C
 ABI calls one to one on torch tensors.
@@ -108,13 +112,17 @@ _ws_cache: dict = {}
 
 
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A zero-filled scratch buffer per device, grown on demand (256-byte
-    aligned, as the caching allocator returns).  The library leaves its counter
-    zero after every completed call.  Calls on concurrent streams of one device
-    must pass their own buffers to the low-level API."""
-    key = (device.type, device.index)
+    """A zero-filled scratch buffer per (device, current stream), grown on
+    demand (256-byte aligned, as the caching allocator returns).  The library
+    leaves its counter zero after every completed call, and calls on one stream
+    run one after another, so a stream's calls can share its buffer; calls on
+    different streams get different buffers and may run at the same time."""
+    stream = torch.cuda.current_stream(device)
+    key = (device.type, device.index, stream.cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
+        # allocated on the stream that will use it: the caching allocator orders
+        # its zero-fill before that stream's later work
         buf = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf

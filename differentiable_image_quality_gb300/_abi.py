@@ -6,6 +6,7 @@ becomes a Python exception.  Every step of the computation runs in libgbssim.so.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -16,7 +17,9 @@ VALID, SAME = 0, 1
 PADDING = {"valid": VALID, "same": SAME}
 
 _lock = threading.Lock()
-_lib = None
+_lib = None       # the product library
+_test_lib = None  # the test build, loaded on request
+_active = None    # the library the package's calls go to (None: the product library)
 
 # names the header declares, with (restype, argtypes)
 _vp, _sz, _i, _fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
@@ -42,9 +45,13 @@ SIGNATURES = {
     "ssim3d_bwd": (_i, [_fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _fp, _sz, _fp, _fp, _vp, _sz,
                         _vp]),
 }
-# exported beyond the header: tuning hooks of the planner and of the input
-# staging (the latter also drives the tests of the bounded-wait failure path)
-EXTRA = {"gbssim_tune_seg_rows": (None, [_i]), "gbssim_tune_staging": (None, [_i])}
+# exported only by the test build (libgbssim_test.so, csrc/gbssim_test_hooks.h):
+# forced row segments, the staging modes that drive the tests of the bounded-wait
+# failure path, and the per-stage statistics dump
+TEST_SIGNATURES = {
+    "gbssim_tune_seg_rows": (None, [_i]),
+    "gbssim_tune_staging": (None, [_i]),
+}
 
 
 class GbssimError(RuntimeError):
@@ -57,10 +64,23 @@ def lib_path() -> str:
     return _build.LIB
 
 
+def _open(path: str, signatures: dict):
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in signatures.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load(build_if_missing: bool = False):
-    """Load libgbssim.so.  Raises when it has not been built (no fallback)."""
+    """The library the package's calls go to: libgbssim.so unless a test has
+    switched to the test build (using_test_library).  Raises when it has not
+    been built (no fallback)."""
     global _lib
     with _lock:
+        if _active is not None:
+            return _active
         if _lib is not None:
             return _lib
         if not os.path.exists(_build.LIB):
@@ -70,13 +90,34 @@ def load(build_if_missing: bool = False):
                 raise RuntimeError(
                     "libgbssim.so is not built: run `python -c \"import __graft_entry__ as g; "
                     "g.build()\"` or differentiable_image_quality_gb300._build.build()")
-        lib = ctypes.CDLL(_build.LIB)
-        for name, (res, args) in {**SIGNATURES, **EXTRA}.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
-        return lib
+        _lib = _open(_build.LIB, SIGNATURES)
+        return _lib
+
+
+def load_test():
+    """The test build libgbssim_test.so (the product ABI plus TEST_SIGNATURES)."""
+    global _test_lib
+    with _lock:
+        if _test_lib is None:
+            if not os.path.exists(_build.TEST_LIB):
+                raise RuntimeError("libgbssim_test.so is not built: run _build.build()")
+            _test_lib = _open(_build.TEST_LIB, {**SIGNATURES, **TEST_SIGNATURES})
+        return _test_lib
+
+
+@contextlib.contextmanager
+def using_test_library():
+    """Route the package's calls to the test build inside the block (tests of
+    the staging hooks); yields that library."""
+    global _active
+    lib = load_test()
+    with _lock:
+        prev, _active = _active, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _active = prev
 
 
 def check(fn: str, status: int) -> None:

@@ -7,6 +7,8 @@
 #include <queue>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gbssim.h"
 #include "common.cuh"
 #include "ssim2d.cuh"
@@ -28,6 +30,17 @@ struct DeviceInfo {
     int occ_comp = 0;          // components mode of the forward
     int occ_multi = 0;         // ... several octaves in one launch
     int occ3d[5] = {0, 0, 0, 0, 0};  // 3D: xy; z forward, gradient, + grad2; adjoint
+};
+
+// An NVTX range named after the entry point, open for the call's host-side work
+// (argument checks, planning, launches), so that a profiler's timeline shows
+// which call issued which kernels.  With no profiler attached both NVTX calls
+// return at once.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
 };
 
 std::mutex g_mutex;
@@ -484,19 +497,6 @@ void gbssim_window(float w[11])
     for (int k = 0; k < kTaps; ++k) w[k] = tap(k);
 }
 
-// Tuning hook for benchmarks: make the 2D planner cut every strip into
-// ceil(rows / `rows`) equal row segments (0 restores the planner; lengths below
-// the planner's minimum are raised to it).  Results do not depend on it.
-void gbssim_tune_seg_rows(int rows)
-{
-    g_seg_rows_override = rows > 0 ? (rows < kMinSegRows ? kMinSegRows : rows) : 0;
-}
-
-// Tuning and test hook of the 2D input staging: 0 tensor copies where the
-// images allow them (the default), 1 cp.async copies only, 2 tensor copies whose
-// waits are made to run out (exercises the bounded-wait failure path).
-void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
-
 int gbssim_device_status(unsigned *flags_out)
 {
     if (!flags_out) return GBSSIM_EINVAL;
@@ -528,6 +528,7 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
              float *out_mean, float *out_map_or_null, float *saved_or_null, size_t saved_bytes,
              int want_grad2, void *workspace, size_t workspace_bytes, void *stream)
 {
+    const CallRange range("ssim_fwd");
     int rc;
     if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_mean)) ||
         (rc = check_opt(out_map_or_null)) || (rc = check_opt(saved_or_null)))
@@ -583,6 +584,7 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
              int padding, const float *saved_or_null, size_t saved_bytes, float *grad_img1,
              float *grad_img2_or_null, void *stream)
 {
+    const CallRange range("ssim_bwd");
     int rc;
     if ((rc = check_in(dL)) || (rc = check_in(img1)) || (rc = check_in(img2)) ||
         (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)) ||
@@ -664,6 +666,7 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
                  int octaves, float *out_means, float *maps_or_null, void *workspace,
                  size_t workspace_bytes, void *stream)
 {
+    const CallRange range("ssim_pyramid");
     int rc;
     if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_means)) ||
         (rc = check_opt(maps_or_null)))
@@ -870,6 +873,7 @@ int ssim3d_fwd(const float *img1, const float *img2, int N, int C, int D, int H,
                size_t saved_bytes, int want_grad2, void *workspace, size_t workspace_bytes,
                void *stream)
 {
+    const CallRange range("ssim3d_fwd");
     int rc;
     if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_mean)) ||
         (rc = check_opt(out_map_or_null)) || (rc = check_opt(saved_or_null)))
@@ -902,6 +906,7 @@ int ssim3d_bwd(const float *dL, const float *img1, const float *img2, int N, int
                float *grad_img1, float *grad_img2_or_null, void *workspace,
                size_t workspace_bytes, void *stream)
 {
+    const CallRange range("ssim3d_bwd");
     int rc;
     if ((rc = check_in(dL)) || (rc = check_in(img1)) || (rc = check_in(img2)) ||
         (rc = check_in(grad_img1)) || (rc = check_opt(grad_img2_or_null)) ||
@@ -952,6 +957,7 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
                  const float *dL, float *out_mean, float *out_map_or_null, float *grad_img1,
                  float *grad_img2_or_null, void *workspace, size_t workspace_bytes, void *stream)
 {
+    const CallRange range("ssim_fwd_bwd");
     int rc;
     if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(dL)) ||
         (rc = check_in(out_mean)) || (rc = check_opt(out_map_or_null)) ||
@@ -1011,6 +1017,7 @@ int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, in
                    float *grad_img1, float *grad_img2_or_null, void *workspace,
                    size_t workspace_bytes, void *stream)
 {
+    const CallRange range("ssim3d_fwd_bwd");
     int rc;
     if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(dL)) ||
         (rc = check_in(out_mean)) || (rc = check_opt(out_map_or_null)) ||
@@ -1041,5 +1048,22 @@ int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, in
     fill3d(a, img1, img2, N, C, D, H, W, padding, workspace);
     return run3d(d, a, N, out_mean, out_map_or_null, true, g2, grad_img1, grad_img2_or_null, dL, s);
 }
+
+#ifdef GBSSIM_TEST_HOOKS
+// ---- test build only (csrc/gbssim_test_hooks.h)
+
+// Make the 2D planner cut every strip into ceil(rows / `rows`) equal row
+// segments (0 restores the planner; lengths below the planner's minimum are
+// raised to it).  Results do not depend on it.
+void gbssim_tune_seg_rows(int rows)
+{
+    g_seg_rows_override = rows > 0 ? (rows < kMinSegRows ? kMinSegRows : rows) : 0;
+}
+
+// Staging of the 2D and 3D kernels: 0 tensor copies where the images allow
+// them (the product behaviour), 1 cp.async copies only, 2 tensor copies whose
+// waits are made to run out (exercises the bounded-wait failure path).
+void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
+#endif
 
 }  // extern "C"

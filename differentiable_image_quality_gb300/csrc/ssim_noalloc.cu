@@ -10,7 +10,6 @@
 // the library itself defines; every GPU that loads the library holds the array
 // (GBSSIM_NOALLOC_SCRATCH_BYTES) until the process exits.
 #include <cstddef>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -20,34 +19,23 @@ namespace {
 
 constexpr size_t kScratchBytes = GBSSIM_NOALLOC_SCRATCH_BYTES;
 constexpr size_t kCounterBytes = 256;  // ssim_fwd keeps its completion counter here
-constexpr int kMaxDevices = 64;
 
 // The scratch.  In host code this name is only a stand-in for the device
 // array: its device address comes from cudaGetSymbolAddress, per device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_lock;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch on the current device.  Looked up on every
+// call and never cached: a cached address would go stale if the application
+// reset the device or its primary context was destroyed and created again.
 int scratch_on_current_device(void **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
         (void)cudaGetLastError();
         return GBSSIM_ECUDA;
     }
-    std::lock_guard<std::mutex> lock(g_lock);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            (void)cudaGetLastError();
-            return GBSSIM_ECUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return GBSSIM_OK;
 }
 
@@ -58,6 +46,8 @@ extern "C" int ssim_fwd_noalloc(const float *img1, const float *img2, int N, int
                                 float *saved_or_null, size_t saved_bytes, int want_grad2,
                                 void *stream)
 {
+    // the size check comes first: a problem beyond the array is refused whatever
+    // the other arguments are, before anything touches the device
     const size_t need = gbssim_workspace_bytes(N, C, H, W, padding);
     if (need == 0)  // invalid shape or padding: let ssim_fwd report which argument
         return ssim_fwd(img1, img2, N, C, H, W, padding, out_mean, out_map_or_null,

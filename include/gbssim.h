@@ -144,14 +144,17 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
  * library, held until the process exits.  It allocates nothing.
  *   - Shapes whose workspace (gbssim_workspace_bytes) would exceed that array
  *     return GBSSIM_ETOOLARGE; use ssim_fwd for them.  A 1 x 3 x 1080 x 1920
- *     pair needs about 35 KB of it.
+ *     pair needs about 35 KB of it.  This size check comes first: such a shape
+ *     returns GBSSIM_ETOOLARGE whatever the other arguments are.  Any other
+ *     argument error is reported as ssim_fwd reports it.
  *   - All calls on a device share the one array and it keeps the previous
- *     call's contents; the call clears the part that must start at zero.  Calls
- *     whose work overlaps on the GPU (other streams, other threads) race on it:
- *     order them on one stream.
- *   - The first call on each device looks up the array's device address (and
- *     does the per-device set-up ssim_fwd also does); make that first call
- *     before any stream capture.
+ *     call's contents; the call clears the part that must start at zero, on
+ *     `stream`, before its kernel.  Calls whose work overlaps on the GPU (other
+ *     streams, other threads) race on it: order them on one stream.
+ *   - Every call looks up the array's address on the current device (nothing
+ *     is cached, so a device reset cannot leave a stale address).  The first
+ *     call on each device also does the per-device set-up ssim_fwd does; make
+ *     that first call before any stream capture.
  * Results are identical to ssim_fwd's. */
 int ssim_fwd_noalloc(const float *img1, const float *img2, int N, int C, int H, int W,
                      int padding, float *out_mean, float *out_map_or_null, float *saved_or_null,

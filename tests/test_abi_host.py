@@ -48,6 +48,27 @@ def test_library_exports_every_declared_symbol(lib):
         assert name in _abi.SIGNATURES, f"{name} has no ctypes signature"
 
 
+def test_product_library_exports_only_the_header(lib):
+    """The test hooks live in the test build; the product library's dynamic
+    symbols are the header's functions and nothing else."""
+    import subprocess
+
+    from differentiable_image_quality_gb300 import _abi, _build
+
+    for hook in _abi.TEST_SIGNATURES:
+        assert not hasattr(lib, hook), f"{hook} is exported by the product library"
+    test_lib = _abi.load_test()
+    for hook in _abi.TEST_SIGNATURES:
+        assert hasattr(test_lib, hook), f"{hook} missing from the test build"
+    try:
+        out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                             text=True, check=True).stdout
+    except (OSError, subprocess.CalledProcessError):
+        pytest.skip("nm not available")
+    exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert exported == declared_functions()
+
+
 def test_abi_version(lib):
     assert lib.gbssim_abi_version() == 1
 

@@ -130,15 +130,15 @@ def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
 
     x, y = uniform_pair((2, 2, 97, 150), 600 + seg_rows, std=0.1)
     dl = np.array([-1.0, -0.3])
-    lib = _abi.load()
-    lib.gbssim_tune_seg_rows(seg_rows)
-    try:
-        for path in ("saved", "recompute"):
-            got = _run(dev, x, y, dl, padding, True, path, want_map=True)
-            ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
-            _assert_parity(got, ref, True, f"seg_rows={seg_rows} {padding} {path}")
-    finally:
-        lib.gbssim_tune_seg_rows(0)
+    with _abi.using_test_library() as lib:  # the segment hook is in the test build only
+        lib.gbssim_tune_seg_rows(seg_rows)
+        try:
+            for path in ("saved", "recompute"):
+                got = _run(dev, x, y, dl, padding, True, path, want_map=True)
+                ref = _oracle(oracle_mod, x, y, dl, padding, True, want_map=True)
+                _assert_parity(got, ref, True, f"seg_rows={seg_rows} {padding} {path}")
+        finally:
+            lib.gbssim_tune_seg_rows(0)
 
 
 @pytest.mark.parametrize("name", ["tiny64_valid", "splat1080_valid", "splat1080_same",

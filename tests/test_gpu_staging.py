@@ -10,7 +10,8 @@ for it, every thread issues cp.async copies.  Both must give the oracle's result
 bounded: when it runs out, the kernel's blocks stop, the device records the
 failure, the affected means come out NaN, and the context stays usable.  The
 hook's mode 2 makes every wait run out by announcing 16 bytes more than the
-copies deliver; no fault is involved.
+copies deliver; no fault is involved.  The hook exists only in the test build
+of the library (libgbssim_test.so), which these tests load.
 """
 import ctypes
 
@@ -27,6 +28,8 @@ STAGING_TIMEOUT = 1  # GBSSIM_DEV_STAGING_TIMEOUT
 
 @pytest.fixture(scope="module")
 def lib():
+    """The test build of the library (the staging hook is not part of the
+    product library); every package call in this module goes to it."""
     import torch
 
     if not torch.cuda.is_available():
@@ -34,7 +37,8 @@ def lib():
     from differentiable_image_quality_gb300 import _abi, _build
 
     _build.build()
-    return _abi.load()
+    with _abi.using_test_library() as test_lib:
+        yield test_lib
 
 
 def _status(lib):

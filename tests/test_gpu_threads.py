@@ -63,3 +63,41 @@ def test_concurrent_calls_on_two_streams():
     for (t, it), (k, (m, g)) in results.items():
         assert np.array_equal(m, alone[k][0]), (t, it, "mean")
         assert np.array_equal(g, alone[k][1]), (t, it, "grad")
+
+
+def test_fused_ssim_autograd_on_two_streams_at_once(oracle_mod):
+    """The autograd API on two streams whose work overlaps on the GPU: each
+    stream gets its own scratch buffer, so both losses and gradients match the
+    oracle."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import differentiable_image_quality_gb300 as pkg
+
+    dev = torch.device("cuda:0")
+    cases = [((2, 3, 300, 410), "valid", 21), ((1, 3, 257, 380), "same", 22)]
+    streams = [torch.cuda.Stream(dev) for _ in cases]
+    inputs, outs = [], []
+    for (shape, padding, seed), s in zip(cases, streams):
+        x, y = uniform_pair(shape, seed, std=0.08)
+        with torch.cuda.stream(s):
+            t1 = torch.from_numpy(x).to(dev).requires_grad_(True)
+            t2 = torch.from_numpy(y).to(dev).requires_grad_(True)
+        inputs.append((x, y, t1, t2))
+    torch.cuda.synchronize()
+    for (shape, padding, _), s, (_, _, t1, t2) in zip(cases, streams, inputs):
+        with torch.cuda.stream(s):  # both forwards queued before either backward
+            outs.append(1.0 - pkg.fused_ssim(t1, t2, padding))
+    for loss, s in zip(outs, streams):
+        with torch.cuda.stream(s):
+            loss.backward()
+    torch.cuda.synchronize()
+    for (shape, padding, _), (x, y, t1, t2), loss in zip(cases, inputs, outs):
+        N = shape[0]
+        ref_mean = oracle_mod.ssim2d(x, y, padding)
+        g1, g2 = oracle_mod.ssim2d_grad(x, y, np.full(N, -1.0 / N), padding)
+        assert abs(float(loss.item()) - (1.0 - float(np.mean(ref_mean)))) <= 1e-5
+        for got, ref in ((t1.grad, g1), (t2.grad, g2)):
+            err = np.max(np.abs(got.cpu().numpy() - ref)) / np.max(np.abs(ref))
+            assert err <= 1e-4, f"{shape} {padding}: gradient error {err:.2e}"

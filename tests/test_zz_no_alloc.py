@@ -52,6 +52,8 @@ def _case(torch, dev, x, y, padding, want_map, want_saved):
 
 
 def _call(torch, lib, dev, case, noalloc):
+    """One forward of `case` on the current stream: through ssim_fwd_noalloc, or
+    through ssim_fwd (the package's wrapper, a workspace of its own)."""
     import differentiable_image_quality_gb300 as pkg
 
     tx, ty = case["x"], case["y"]
@@ -99,11 +101,30 @@ def test_noalloc_forward_matches_ssim_fwd_on_two_calls_in_a_row(env):
     _compare(again, refs[0])
 
 
+def test_noalloc_forward_on_a_stream_of_its_own(env):
+    """Two calls queued back to back on a stream the test creates (not the
+    legacy default stream): the clearing of the array and each kernel stay in
+    order on that stream, so both results match ssim_fwd's."""
+    torch, lib, dev = env
+    x1, y1 = uniform_pair((1, 3, 130, 260), 902, std=0.05)
+    x2, y2 = uniform_pair((3, 1, 64, 77), 903, std=0.2)
+    cases = [_case(torch, dev, x1, y1, "valid", True, False),
+             _case(torch, dev, x2, y2, "same", False, True)]
+    refs = [_call(torch, lib, dev, c, noalloc=False) for c in cases]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        got = [_call(torch, lib, dev, c, noalloc=True) for c in cases]
+    side.synchronize()
+    for g, r in zip(got, refs):
+        _compare(g, r)
+
+
 def test_noalloc_forward_rejects_problems_beyond_its_scratch(env):
     _, lib, _ = env
-    # 64 RGB 1080p images need more than the 1 MiB array: refused before any work
-    fake = 1 << 30
-    st = lib.ssim_fwd_noalloc(fake, 2 * fake, 64, 3, 1080, 1920, 0, 3 * fake, None, None, 0, 0,
-                              None)
+    # 64 RGB 1080p images need more than the 1 MiB array: refused by the size
+    # check, which comes first; the null pointers are never reached (were the
+    # check to break, ssim_fwd's own null-pointer check would refuse them too)
+    st = lib.ssim_fwd_noalloc(None, None, 64, 3, 1080, 1920, 0, None, None, None, 0, 0, None)
     assert st == ETOOLARGE
     assert b"ssim_fwd_noalloc" in lib.gbssim_strerror(st)
