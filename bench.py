@@ -134,14 +134,19 @@ class ClockSampler:
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [r for r in rows if r[2] > 200.0] or rows
+        # "under load": samples drawing more than 200 W; if none did (a short
+        # run between samples), the figures are over all samples, and say so
+        loaded = [r for r in rows if r[2] > 200.0]
+        basis = loaded or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:])
+        reasons = sorted({names[i] for r in basis for i, v in enumerate(r[3][1:])
                           if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded),
-                "sm_max_mhz": max(r[1] for r in loaded),
-                "power_w_max": max(r[2] for r in loaded),
+        return {"sm_mhz": statistics.median(r[0] for r in basis),
+                "sm_max_mhz": max(r[1] for r in basis),
+                "power_w_max": max(r[2] for r in rows),
                 "samples": len(rows), "samples_under_load": len(loaded),
+                "sm_mhz_basis": "samples above 200 W" if loaded else
+                                "all samples (none above 200 W)",
                 "reasons": reasons}
 
 
@@ -298,40 +303,39 @@ def profiled_traffic(path=PROFILE):
     return float(m.group(1))
 
 
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
-
-    import differentiable_image_quality_gb300 as pkg
+def workload_setup(pkg, torch, dev, name):
+    """Device inputs and outputs of one workload, and its per-step call closures."""
     from workloads import WORKLOADS, dl_vector, make_inputs
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pkg._abi.load()
-    name = args.workload
     wl = WORKLOADS[name]
     is3d = wl.ndim == 3
-    unit = UNIT if not is3d else "Mvoxel/s"
     x, y = make_inputs(name)
     dl = dl_vector(name)
-    N, C = x.shape[:2]
-    elems = x.size
-    mp = units(x.shape)
+    N = x.shape[0]
     g2wanted = wl.want_grad2
     fwd_call = pkg.ssim3d_fwd if is3d else pkg.ssim_fwd
     bwd_call = pkg.ssim3d_bwd if is3d else pkg.ssim_bwd
     fused_call = pkg.ssim3d_fwd_bwd if is3d else pkg.ssim_fwd_bwd
-
     tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
     tdl = torch.from_numpy(dl).to(dev)
     mean = torch.empty(N, device=dev)
     saved = torch.empty(pkg.saved_bytes(x.shape, g2wanted) // 4, device=dev)
     g1 = torch.empty_like(tx)
     g2 = torch.empty_like(ty) if g2wanted else None
-    flush = torch.empty(FLUSH_BYTES // 4, device=dev)
+    w = {"wl": wl, "x": x, "y": y, "tx": tx, "ty": ty, "tdl": tdl, "mean": mean, "saved": saved,
+         "g1": g1, "g2": g2, "fwd": fwd_call, "bwd": bwd_call, "is3d": is3d,
+         "mp": units(x.shape), "elems": x.size}
+    w["fwd_train"] = lambda: fwd_call(tx, ty, wl.padding, mean, saved=saved, want_grad2=g2wanted)
+    w["bwd_saved"] = lambda: bwd_call(tdl, tx, ty, wl.padding, g1, g2, saved=saved)
+    w["fwd_infer"] = lambda: fwd_call(tx, ty, wl.padding, mean)
+    w["bwd_recompute"] = lambda: bwd_call(tdl, tx, ty, wl.padding, g1, g2)
+    w["single_call"] = lambda: fused_call(tx, ty, wl.padding, tdl, mean, g1, g2)
+    return w
+
+
+def make_timer(torch, dev, world, flush):
+    import torch.distributed as dist
+
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn_a, fn_b, steps, warmup):
@@ -362,22 +366,78 @@ def run_ours(args):
         tb = [e[1].elapsed_time(e[2]) for e in ev]
         return ta, tb
 
-    def fwd_train():
-        fwd_call(tx, ty, wl.padding, mean, saved=saved, want_grad2=g2wanted)
+    return timed
 
-    def bwd_saved():
-        bwd_call(tdl, tx, ty, wl.padding, g1, g2, saved=saved)
+
+def roofline_figures(w, step_ms, fwd_ms, peaks, alu_peak_tflops):
+    """Minimal HBM bytes of a forward + backward step and its fraction of the
+    measured copy peak; the training forward's flops and its fraction of the
+    fp32 ALU peak."""
+    elems = w["elems"]
+    grads = 2 if w["wl"].want_grad2 else 1
+    min_bytes = (2 * elems + 2 * elems + grads * elems) * 4  # fwd: read 2; bwd: read 2, write grads
+    flops_px = GRAD3D_FLOPS_PER_VOXEL if w["is3d"] else GRAD_FLOPS_PER_PIXEL
+    achieved_tflops = flops_px * elems / (fwd_ms / 1e3) / 1e12
+    hbm_gbs = min_bytes / (step_ms / 1e3) / 1e9
+    return {"min_bytes": min_bytes, "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"],
+            "flops_px": flops_px, "tflops": achieved_tflops,
+            "alu_frac": achieved_tflops / alu_peak_tflops}
+
+
+def workload_summary(w, timed, steps, peaks, alu_peak_tflops):
+    """The step and its parts on one workload (fewer steps than the headline)."""
+    step_ms, _ = timed(lambda: (w["fwd_train"](), w["bwd_saved"]()), None, steps, 3)
+    ta, tb = timed(w["fwd_train"], w["bwd_saved"], steps, 3)
+    ra, rb = timed(w["fwd_infer"], w["bwd_recompute"], steps, 3)
+    sa, _ = timed(w["single_call"], None, steps, 3)
+    mp = w["mp"]
+    st, fw = statistics.mean(step_ms), statistics.mean(ta)
+    rf = roofline_figures(w, st, fw, peaks, alu_peak_tflops)
+    return {"shape": list(w["x"].shape), "padding": w["wl"].padding,
+            "grads": "img1, img2" if w["wl"].want_grad2 else "img1",
+            "fwd_bwd_mps": mp / (st / 1e3), "us_per_step": 1e3 * st,
+            "fwd_mps": mp / (fw / 1e3), "bwd_mps": mp / (statistics.mean(tb) / 1e3),
+            "fwd_infer_mps": mp / (statistics.mean(ra) / 1e3),
+            "bwd_recompute_mps": mp / (statistics.mean(rb) / 1e3),
+            "single_call_fwd_bwd_mps": mp / (statistics.mean(sa) / 1e3),
+            "hbm_frac": rf["hbm_frac"], "alu_frac": rf["alu_frac"], "steps": steps}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import differentiable_image_quality_gb300 as pkg
+    from workloads import WORKLOADS
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg._abi.load()
+    name = args.workload
+    w = workload_setup(pkg, torch, dev, name)
+    wl, x, is3d, mp, elems = w["wl"], w["x"], w["is3d"], w["mp"], w["elems"]
+    unit = UNIT if not is3d else "Mvoxel/s"
+    N = x.shape[0]
+    g2wanted = wl.want_grad2
+    fwd_call, bwd_call = w["fwd"], w["bwd"]
+    mean, saved, g1, g2, tdl = w["mean"], w["saved"], w["g1"], w["g2"], w["tdl"]
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    timed = make_timer(torch, dev, world, flush)
 
     def train_step():
-        fwd_train()
-        bwd_saved()
+        w["fwd_train"]()
+        w["bwd_saved"]()
 
     # the step as a whole (no event between forward and backward, so the
     # backward's launch may overlap the forward's tail), then the two halves
     with ClockSampler(local) as clocks:
         step_ms, _ = timed(train_step, None, args.steps, max(3, args.warmup))
     clk = clocks.summary()
-    ta, tb = timed(fwd_train, bwd_saved, args.steps, 3)
+    ta, tb = timed(w["fwd_train"], w["bwd_saved"], args.steps, 3)
 
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     value = whole_job_rate(mp, world, args.steps, total_ms)
@@ -393,7 +453,7 @@ def run_ours(args):
     # copy per step (img1 and img2 are its two halves)
     hxy = torch.empty((2,) + tuple(x.shape), dtype=torch.float32).pin_memory()
     hxy[0].copy_(torch.from_numpy(x))
-    hxy[1].copy_(torch.from_numpy(y))
+    hxy[1].copy_(torch.from_numpy(w["y"]))
     hg1 = torch.empty(x.shape, dtype=torch.float32).pin_memory()
     hg2 = torch.empty(x.shape, dtype=torch.float32).pin_memory() if g2wanted else None
     hm = torch.empty(N, dtype=torch.float32).pin_memory()
@@ -451,19 +511,17 @@ def run_ours(args):
     ts_, _ = timed(e2e_serial_step, None, args.steps, max(3, args.warmup))
     e2e_serial_value = whole_job_rate(mp, world, args.steps, max_over_ranks(sum(ts_), world, dev))
 
+    peaks, peak_kind = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sm_count = props.multi_processor_count
+    sm_max = float(clk.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0))
+    alu_peak_tflops = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
+
     extras = {}
+    workloads = {}
     if not args.no_extras:
-        def fwd_infer():
-            fwd_call(tx, ty, wl.padding, mean)
-
-        def bwd_recompute():
-            bwd_call(tdl, tx, ty, wl.padding, g1, g2)
-
-        def single_call():
-            fused_call(tx, ty, wl.padding, tdl, mean, g1, g2)
-
-        ra, rb = timed(fwd_infer, bwd_recompute, args.steps, 3)
-        sa, _ = timed(single_call, None, args.steps, 3)
+        ra, rb = timed(w["fwd_infer"], w["bwd_recompute"], args.steps, 3)
+        sa, _ = timed(w["single_call"], None, args.steps, 3)
         pyr = {}
         if not is3d:
             # the per-octave stage: l, cs and S means of every octave (maps not written)
@@ -473,6 +531,7 @@ def run_ours(args):
                     11 if wl.padding == "valid" else 1):
                 octs += 1
             pyr_means = torch.empty((octs, 3, N), device=dev)
+            tx, ty = w["tx"], w["ty"]
 
             def pyramid():
                 pkg.ssim_pyramid(tx, ty, wl.padding, octs, out_means=pyr_means)
@@ -489,32 +548,44 @@ def run_ours(args):
             "single_call_fwd_bwd_mps": mp / (statistics.mean(sa) / 1e3),
             **pyr,
         }
+        # every other workload of the suite, fewer steps each (rank 0's GPU only
+        # matters for the line; every rank runs them so that collectives stay matched)
+        for other in WORKLOADS:
+            if other == name:
+                continue
+            wo = workload_setup(pkg, torch, dev, other)
+            workloads[other] = workload_summary(wo, timed, max(10, min(args.steps, 50)), peaks,
+                                                alu_peak_tflops)
+            del wo
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peaks, peak_kind = measured_peaks()
-    props = torch.cuda.get_device_properties(dev)
-    sm_count = props.multi_processor_count
-    sm_max = float(clk.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0))
-    alu_peak_tflops = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
-    flops_px = GRAD_FLOPS_PER_PIXEL if not is3d else GRAD3D_FLOPS_PER_VOXEL
-    achieved_tflops = flops_px * elems / (fwd_ms / 1e3) / 1e12
-    grads = 2 if g2wanted else 1
-    min_bytes = (2 * elems + 2 * elems + grads * elems) * 4  # fwd: read 2; bwd: read 2, write grads
-    step_s = statistics.mean(step_ms) / 1e3
-    hbm_gbs = min_bytes / step_s / 1e9
+    step_mean = statistics.mean(step_ms)
+    rf = roofline_figures(w, step_mean, fwd_ms, peaks, alu_peak_tflops)
+    workloads[name] = {
+        "shape": list(x.shape), "padding": wl.padding,
+        "grads": "img1, img2" if g2wanted else "img1",
+        "fwd_bwd_mps": mp / (step_mean / 1e3), "us_per_step": 1e3 * step_mean,
+        "fwd_mps": mp / (fwd_ms / 1e3), "bwd_mps": mp / (bwd_ms / 1e3),
+        **({"fwd_infer_mps": extras["fwd_infer_mps"],
+            "bwd_recompute_mps": extras["bwd_recompute_mps"],
+            "single_call_fwd_bwd_mps": extras["single_call_fwd_bwd_mps"]} if extras else {}),
+        "hbm_frac": rf["hbm_frac"], "alu_frac": rf["alu_frac"], "steps": args.steps}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(name, unit)
 
+    traffic = (profiled_traffic() if name == WORKLOAD else
+               profiled_traffic(PROFILE3D) if name == "volume128_valid" else None)
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup),
-        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
+        "ms_per_step": step_mean, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": name, "shape": list(x.shape), "padding": wl.padding,
                    "grads": "img1, img2" if g2wanted else "img1",
@@ -526,15 +597,18 @@ def run_ours(args):
         # per step: the forward kernel(s) (2D: one; 3D: xy, z, adjoint) and the scaling backward
         "gpu_launches": (2 if not is3d else 4) * args.steps,
         "roofline": {"kernel": KERNEL_NAME if not is3d else KERNEL3D_NAME, "bound": "alu",
-                     "achieved": achieved_tflops, "peak": alu_peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved_tflops / alu_peak_tflops,
-                     "traffic": (profiled_traffic() if name == WORKLOAD else
-                                 profiled_traffic(PROFILE3D) if name == "volume128_valid" else None),
+                     "achieved": rf["tflops"], "peak": alu_peak_tflops, "unit": "TFLOP/s",
+                     "frac": rf["alu_frac"],
+                     "traffic": traffic,
+                     "traffic_source": ("ncu capture of the same kernel sources, per launch, from "
+                                        "the committed profile summary (not measured in this run)"
+                                        if traffic is not None else
+                                        "no ncu capture of the current kernel sources"),
                      "peak_basis": f"{sm_count} SMs x 128 fp32 lanes x 2 flops x {sm_max:.0f} MHz",
-                     "flops_per_pixel": flops_px},
-        "hbm_roofline": {"min_bytes_per_step": min_bytes, "achieved_gbs": hbm_gbs,
-                         "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
-                         "frac_of_measured": hbm_gbs / peaks["hbm_gbs"],
+                     "flops_per_pixel": rf["flops_px"]},
+        "hbm_roofline": {"min_bytes_per_step": rf["min_bytes"], "achieved_gbs": rf["hbm_gbs"],
+                         "frac_of_8tbs": rf["hbm_gbs"] / NOMINAL_HBM_GBS,
+                         "frac_of_measured": rf["hbm_frac"],
                          "measured_peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "e2e": {"value": e2e_value, "unit": unit,
@@ -546,10 +620,11 @@ def run_ours(args):
                 "serial_with_gradient_readback": {
                     "value": e2e_serial_value, "unit": unit,
                     "h2d_bytes_per_step": 2 * elems * 4,
-                    "d2h_bytes_per_step": grads * elems * 4 + N * 4}},
+                    "d2h_bytes_per_step": (2 if g2wanted else 1) * elems * 4 + N * 4}},
         "clocks": clk,
         "cpu_baseline": cpu,
         **extras,
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -28,11 +28,15 @@ constexpr int kRadius = 5;
 constexpr float kC1 = 1.0e-4f;  // (0.01 * 1)^2
 constexpr float kC2 = 9.0e-4f;  // (0.03 * 1)^2
 
-// Every value enters the products as (v - kShift), the image being extended
-// by zeros, i.e. the shifted image by -kShift.  The variances and covariance are
-// invariant under a common shift of the window's values when the window's
-// weights sum to one, which they do once the zero extension is counted; the
-// shift only reduces float32 cancellation in E[x^2] - mu^2 (values in [0, 1]).
+// Values enter the products shifted: x' = x - s, y' = y - t, the image being
+// extended by zeros, i.e. the shifted image by -s (-t).  The variances and
+// covariance are invariant under a common shift of a window's values when the
+// window's weights sum to one, which they do once the zero extension is
+// counted; the shift only reduces float32 cancellation in E[x'^2] - E[x']^2,
+// which is smallest when s is close to the window's own values.  The 2D kernels
+// take s and t from one in-image pixel near each 11-row band of an 8-column
+// group of windows (the shift is exact for any value, as long as all pixels of
+// one window share it); the 3D kernels use the constant kShift.
 constexpr float kShift = 0.5f;
 
 // ------------------------------------------------------------ cp.async helpers
@@ -165,7 +169,8 @@ __device__ __forceinline__ float rcp_approx(float x)
 // ------------------------------------------------------------ SSIM at a pixel
 
 // Statistics of one window in shifted form: m1 = E[x'], m2 = E[y'],
-// es = E[x'^2] + E[y'^2], e12 = E[x'y'], with x' = x - kShift, y' = y - kShift.
+// es = E[x'^2] + E[y'^2], e12 = E[x'y'], with x' = x - s, y' = y - t for the
+// window's shift sh = (s, t).
 struct Moments {
     float m1, m2, es, e12;
 };
@@ -178,13 +183,13 @@ struct MomentGrads {
 };
 
 // S = A1 A2 / (B1 B2) with
-//   mu = m + kShift, sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2,
+//   mu = m + sh, sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2,
 //   A1 = 2 mu1 mu2 + C1, A2 = 2 sigma12 + C2, B1 = mu1^2 + mu2^2 + C1,
 //   B2 = sigma_sum + C2.
-__device__ __forceinline__ float ssim_value(const Moments &m)
+__device__ __forceinline__ float ssim_value(const Moments &m, float2 sh)
 {
     const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 mu = __fadd2_rn(M, sh);
     const float2 msq = __fmul2_rn(M, M);
     const float2 musq = __fmul2_rn(mu, mu);
     const float ss = m.es - (msq.x + msq.y);
@@ -197,10 +202,10 @@ __device__ __forceinline__ float ssim_value(const Moments &m)
 }
 
 // The two factors of S: (l, cs) = (A1 / B1, A2 / B2), S = l * cs.
-__device__ __forceinline__ float2 ssim_factors(const Moments &m)
+__device__ __forceinline__ float2 ssim_factors(const Moments &m, float2 sh)
 {
     const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 mu = __fadd2_rn(M, sh);
     const float2 msq = __fmul2_rn(M, M);
     const float2 musq = __fmul2_rn(mu, mu);
     const float ss = m.es - (msq.x + msq.y);
@@ -222,10 +227,11 @@ __device__ __forceinline__ float2 ssim_factors(const Moments &m)
 // When `valid` is false every derivative (and S) comes out as exactly zero:
 // l and cs are zeroed before they are used.
 template <bool WANT_G2>
-__device__ __forceinline__ float ssim_and_grads(const Moments &m, bool valid, MomentGrads &g)
+__device__ __forceinline__ float ssim_and_grads(const Moments &m, float2 sh, bool valid,
+                                                MomentGrads &g)
 {
     const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, make_float2(kShift, kShift));
+    const float2 mu = __fadd2_rn(M, sh);
     const float2 msq = __fmul2_rn(M, M);
     const float2 musq = __fmul2_rn(mu, mu);
     const float ss = m.es - (msq.x + msq.y);

@@ -1064,6 +1064,48 @@ void gbssim_tune_seg_rows(int rows)
 // them (the product behaviour), 1 cp.async copies only, 2 tensor copies whose
 // waits are made to run out (exercises the bounded-wait failure path).
 void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
+
+// The gradient-mode kernel (with grad2) of ssim_fwd's stored variant, writing
+// besides the two gradient fields of the means (dL = 1) the window statistics
+// and the derivatives of S of every output pixel: stage-by-stage parity.
+int gbssim_test_stage_dump2d(const float *img1, const float *img2, int N, int C, int H, int W,
+                             int padding, float *out_stats, float *out_grads, float *field1,
+                             float *field2, void *stream)
+{
+    int rc;
+    if ((rc = check_in(img1)) || (rc = check_in(img2)) || (rc = check_in(out_stats)) ||
+        (rc = check_in(out_grads)) || (rc = check_in(field1)) || (rc = check_in(field2)))
+        return rc;
+    if (padding != GBSSIM_VALID && padding != GBSSIM_SAME_ZERO) return GBSSIM_EINVAL;
+    if (!shape2d_ok(N, C, H, W, padding)) return GBSSIM_ESHAPE;
+    if ((reinterpret_cast<uintptr_t>(out_stats) | reinterpret_cast<uintptr_t>(out_grads)) % 16)
+        return GBSSIM_EALIGN;
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    const int Ho = out_extent(H, padding), Wo = out_extent(W, padding);
+    const int off = padding == GBSSIM_VALID ? 0 : kRadius;
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
+                                   d->occ2d[2]);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    Ssim2dArgs a{};
+    a.x = img1; a.y = img2;
+    a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
+    a.off = off;
+    a.C = C;
+    set_segments(a, p, H);
+    a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    ssim2d_prepare_staging(a, (long long)N * C, true);
+    a.out1 = field1;
+    a.out2 = field2;
+    a.inv_count = float(1.0 / (double(C) * double(Ho) * double(Wo)));
+    a.dump_stats = out_stats;
+    a.dump_grads = out_grads;
+    a.images = N;
+    a.blocks_per_image = int(p.blocks / N);
+    a.count = double(C) * double(Ho) * double(Wo);
+    return cuda_fail(ssim2d_dump_launch(a, int(p.blocks), static_cast<cudaStream_t>(stream)));
+}
 #endif
 
 }  // extern "C"

@@ -21,6 +21,19 @@ void gbssim_tune_seg_rows(int rows);
  * staging wait runs out (the failure path: NaN means, the device status bit). */
 void gbssim_tune_staging(int mode);
 
+/* Stage-by-stage parity of the 2D gradient kernel: one run of the kernel of
+ * ssim_fwd's stored variant with grad2 on img1 / img2 ([N, C, H, W] float32,
+ * device) that also writes, for every output pixel of [N, C, Ho, Wo]:
+ *   out_stats  float4 (mu1, mu2, sigma11 + sigma22, sigma12) of the window;
+ *   out_grads  float4 (dS/dmu1, dS/dmu2, dS/dE[x^2] = dS/dE[y^2], dS/dE[xy]),
+ *              the derivatives of S with respect to the unshifted moments;
+ * both 16-byte aligned, and the two gradient fields of the per-image means
+ * (dL = 1) into field1 / field2 ([N, C, H, W] each).  No mean is reduced.
+ * Returns a gbssim status. */
+int gbssim_test_stage_dump2d(const float *img1, const float *img2, int N, int C, int H, int W,
+                             int padding, float *out_stats, float *out_grads, float *field1,
+                             float *field2, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -204,10 +204,11 @@ constexpr int min_blocks() { return (GRAD && G2) ? 2 : 3; }
 // The work of one block (block = its index in the launch's plan of `a`).  With
 // MULTI the block's partial sums are written but the means are left to the
 // caller (one finish for several octaves in one launch).
-template <bool GRAD, bool G2, bool COMP, bool MULTI>
+template <bool GRAD, bool G2, bool COMP, bool MULTI, bool DUMP = false>
 __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
 {
     static_assert(!(COMP && GRAD), "components mode is forward only");
+    static_assert(!DUMP || (GRAD && G2), "the statistics dump runs in gradient mode with grad2");
     constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
     constexpr int NGH = SW / KH;
     static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
@@ -348,6 +349,25 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         }
     };
 
+    // ---- the shift (s, t) of the windows of row-pass group g whose statistics
+    //      complete in step t: the pixel pair at the first row of block t and
+    //      the middle column of the group's input columns, moved into the image
+    //      (a block wholly outside the image, all zeros, takes 0).  Every window
+    //      of the group that completes in this step lies around that pixel, so
+    //      in a flat region the shifted values are close to zero.  H(t) and V(t)
+    //      read the same staged element while block t is resident.  The value
+    //      is clamped to [0, 1] (NaN gives 0): any shift is exact, and a finite
+    //      one keeps a NaN or infinite pixel from reaching windows that do not
+    //      contain it (through the ring's rebasing).
+    auto shift_of = [&](int t, int g) -> float2 {
+        const int rb = R0 + t * STEP;
+        const int kk = min(max(rb, 0), a.H - 1) - rb;
+        if (kk < 0 || kk >= STEP) return f2(0.f, 0.f);
+        const int cc = min(max(ic0 + g * KH + (KH + 9) / 2, 0), a.W - 1) - ic0;
+        const int i = (t % NBUF) * XB + kk * IWP + cc;
+        return f2(fminf(fmaxf(xs[i], 0.f), 1.f), fminf(fmaxf(ys[i], 0.f), 1.f));
+    };
+
     // ---- row pass of the statistics: row k of block t, columns [KH g, KH g + KH)
     auto h_item = [&](int t, int item) {
         const int g = item / STEP, k = item - g * STEP;
@@ -366,10 +386,12 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             xv[KH + 8] = u.x; xv[KH + 9] = u.y;
             yv[KH + 8] = v.x; yv[KH + 9] = v.y;
         }
+        const float2 sh = shift_of(t, g);
+        const float2 nsh = f2(-sh.x, -sh.y);
         float2 accA[KH], accB[KH];  // (m1, m2), (es, e12)
 #pragma unroll
         for (int m = 0; m < KH + 10; ++m) {
-            const float2 p = f2(xv[m] - kShift, yv[m] - kShift);
+            const float2 p = __fadd2_rn(f2(xv[m], yv[m]), nsh);
             const float2 sq = __fmul2_rn(p, p);
             const float2 q = f2(sq.x + sq.y, p.x * p.y);
 #pragma unroll
@@ -454,7 +476,10 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
                 }
             }
         }
-        // chain rule with the prefetched pixels (cb columns jj + CBOFF: 8-byte aligned)
+        // chain rule with the prefetched pixels (cb columns jj + CBOFF: 8-byte
+        // aligned), in the form grad1 = B^T g~_m1 + 2 (x - 1/2) B^T g_e +
+        // (y - 1/2) B^T g_e12: each window's own shift is folded into g~_m1 (and
+        // g~_m2) by the column pass, so the pixels here all take 1/2
         const float *px = cbx + k * CBP + CBOFF + g * KA;
         const float *py = cby + k * CBP + CBOFF + g * KA;
         float r1[KA], r2[KA];
@@ -525,6 +550,26 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         for (int i = tid; i < n4; i += NT) hb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     int klo = 0, khi = 0, kown = 0;  // rows k of the current step: valid in [klo, khi), owned from kown
+    float2 sh = f2(0.f, 0.f);        // shift of this column's windows completing in the current step
+
+    // The ring's entries of the previous step were formed at that step's shift;
+    // move them to the new one (d = old - new): with x' = x - s_old,
+    //   E[x' + dx] = m1 + dx,  E[(x' + dx)^2] = E[x'^2] + dx (2 m1 + dx),
+    //   E[(x' + dx)(y' + dy)] = e12 + dx (m2 + dy) + dy m1,
+    // exact because every row-pass window's weights sum to one.  Entry 0 is
+    // overwritten by the step's first row before any sum reads it.
+    auto rebase_ring = [&](float2 d) {
+#pragma unroll
+        for (int k = 1; k < STEP; ++k) {
+            const float2 m = hA[k];
+            const float2 v = __fmul2_rn(__ffma2_rn(f2(2.f, 2.f), m, d), d);
+            float2 e = hB[k];
+            e.x = (e.x + v.x) + v.y;
+            e.y = fmaf(d.y, m.x, fmaf(d.x, m.y + d.y, e.y));
+            hB[k] = e;
+            hA[k] = __fadd2_rn(m, d);
+        }
+    };
 
     // ---- prologue
     if (a.tma) {
@@ -577,20 +622,40 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         const Moments mo{M.x, M.y, E.x, E.y};
         if (GRAD) {
             MomentGrads gg;
-            const float S = ssim_and_grads<G2>(mo, ok, gg);
-            gA[k] = f2(gg.g_m1, gg.g_e);
-            if (G2) gB[k] = f2(gg.g_e12, gg.g_m2);
-            else gC[k] = gg.g_e12;
+            const float S = ssim_and_grads<G2>(mo, sh, ok, gg);
+            // fold the window's shift into the first map (the chain rule uses
+            // x - 1/2, y - 1/2 for every pixel):
+            //   g~_m1 = g_m1 + 2 (1/2 - s) g_e + (1/2 - t) g_e12   (g~_m2 likewise)
+            const float g1 = fmaf(1.0f - 2.0f * sh.x, gg.g_e, fmaf(0.5f - sh.y, gg.g_e12, gg.g_m1));
+            gA[k] = f2(g1, gg.g_e);
+            if (G2) {
+                const float g2 = fmaf(1.0f - 2.0f * sh.y, gg.g_e, fmaf(0.5f - sh.x, gg.g_e12, gg.g_m2));
+                gB[k] = f2(gg.g_e12, g2);
+            } else {
+                gC[k] = gg.g_e12;
+            }
+            const bool own = ok && col_own && (k >= kown);
             if (want_mean) {
-                const bool own = ok && col_own && (k >= kown);
                 ssum += own ? S : 0.0f;
                 if (a.map && own) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
+            }
+            if (DUMP && own) {
+                // the window's statistics and the derivatives of S with respect
+                // to the unshifted moments mu1, mu2, E[x^2] (= E[y^2]), E[xy]
+                const size_t o = (size_t(plane) * a.Ho + p) * a.Wo + pc;
+                const float ss = mo.es - (mo.m1 * mo.m1 + mo.m2 * mo.m2);
+                const float s12 = fmaf(-mo.m1, mo.m2, mo.e12);
+                reinterpret_cast<float4 *>(a.dump_stats)[o] =
+                    make_float4(mo.m1 + sh.x, mo.m2 + sh.y, ss, s12);
+                const float dmu1 = fmaf(-2.0f * sh.x, gg.g_e, fmaf(-sh.y, gg.g_e12, gg.g_m1));
+                const float dmu2 = fmaf(-2.0f * sh.y, gg.g_e, fmaf(-sh.x, gg.g_e12, gg.g_m2));
+                reinterpret_cast<float4 *>(a.dump_grads)[o] = make_float4(dmu1, dmu2, gg.g_e, gg.g_e12);
             }
             va[k * P2 + tid] = ring_sum2<k>(gA);
             if (G2) vb2[k * P2 + tid] = ring_sum2<k>(gB);
             else vc[k * P1 + tid] = ring_sum1<k>(gC);
         } else if (COMP) {
-            const float2 lc = ssim_factors(mo);
+            const float2 lc = ssim_factors(mo, sh);
             const float S = lc.x * lc.y;
             lsum += ok ? lc.x : 0.0f;
             csum += ok ? lc.y : 0.0f;
@@ -602,7 +667,7 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
                 m[2 * a.map_stride] = S;
             }
         } else {
-            const float S = ssim_value(mo);
+            const float S = ssim_value(mo, sh);
             ssum += ok ? S : 0.0f;
             if (a.map && ok) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
         }
@@ -615,8 +680,11 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         klo = max(max(0, R0 + 10 - rb), -pb);
         khi = min(min(STEP, Rend - rb), a.Ho - pb);
         kown = (GRAD && seg != 0) ? q0 + 10 - rb : 0;  // q = r - 10 >= q0
-        // ---- V: column passes of step t
+        // ---- V: column passes of step t, at the step's shift
         if (v_warp) {
+            const float2 nsh = shift_of(t, tid / KH);
+            if (t > 0) rebase_ring(f2(sh.x - nsh.x, sh.y - nsh.y));
+            sh = nsh;
             v_row(std::integral_constant<int, 0>{}, t);
             v_row(std::integral_constant<int, 1>{}, t);
             v_row(std::integral_constant<int, 2>{}, t);
@@ -705,6 +773,14 @@ __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
 {
     stream_body<GRAD, G2, COMP, false>(a, blockIdx.x);
 }
+
+#ifdef GBSSIM_TEST_HOOKS
+__global__ void __launch_bounds__(NT, min_blocks<true, true>())
+    ssim2d_dump_kernel(const __grid_constant__ Ssim2dArgs a)
+{
+    stream_body<true, true, false, false, true>(a, blockIdx.x);
+}
+#endif
 
 // Components mode for several octaves in one launch: block b belongs to the
 // octave o with first[o] <= b < first[o + 1]; the last block to finish reduces
@@ -1064,6 +1140,18 @@ const void *ssim2d_components_multi_kernel_ptr()
 {
     return reinterpret_cast<const void *>(ssim2d_components_multi_kernel);
 }
+
+#ifdef GBSSIM_TEST_HOOKS
+cudaError_t ssim2d_dump_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s)
+{
+    const size_t smem = smem_bytes(true, true);
+    const cudaError_t e =
+        cudaFuncSetAttribute(ssim2d_dump_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    ssim2d_dump_kernel<<<blocks, NT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+#endif
 
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)
 {

@@ -36,6 +36,9 @@ struct Ssim2dArgs {
     float *map;       // [planes, Ho, Wo] or null
     size_t map_stride;  // components mode: floats from the l map to the cs map (cs to S)
     int segments;       // blocks of the launch (components mode: partials are [3][segments])
+    // test build only: per output pixel, float4 statistics (mu1, mu2, sigma11 +
+    // sigma22, sigma12) and float4 derivatives of S (see ssim2d_dump_launch)
+    float *dump_stats, *dump_grads;
     // mean reduction (null partials: no mean)
     double *partials;
     unsigned *counter;
@@ -102,6 +105,14 @@ struct OctaveChainArgs {
     long long planes;
 };
 cudaError_t octave_chain_launch(const OctaveChainArgs &m, cudaStream_t s);
+
+#ifdef GBSSIM_TEST_HOOKS
+// Test build: the gradient-mode kernel with grad2 that also writes, for every
+// output pixel it owns, the window statistics and the derivatives of S with
+// respect to the unshifted moments (mu1, mu2, E[x^2] = E[y^2], E[xy]) into
+// a.dump_stats / a.dump_grads ([planes][Ho][Wo] float4 each).
+cudaError_t ssim2d_dump_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s);
+#endif
 
 // g = f * dL[i / per_image] * inv_count for one or two fields (f2/g2 may be null).
 cudaError_t scale_fields_launch(const float *f1, const float *f2, float *g1, float *g2,

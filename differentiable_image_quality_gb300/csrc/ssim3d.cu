@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
         float S;
         if (GRAD) {
             MomentGrads g;
-            S = ssim_and_grads<G2>(mo, true, g);
+            S = ssim_and_grads<G2>(mo, make_float2(kShift, kShift), true, g);
             const float2 vA = zshift2(QA, f2(g.g_m1, g.g_e));
             float2 vB = f2(0.f, 0.f);
             float v12 = 0.f;
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
             else v12 = zshift1(QC, g.g_e12);
             emit(p, vA, vB, v12);
         } else {
-            S = ssim_value(mo);
+            S = ssim_value(mo, make_float2(kShift, kShift));
         }
         if (own && col_ok) {
             ssum += S;

@@ -3,11 +3,16 @@
 Every call goes through the C ABI (via the thin torch wrappers).  Bars, from
 the loss's specification: |mean_gpu - mean_oracle| <= 1e-5 for every image;
 max |grad_gpu - grad_oracle| <= 1e-4 * max |grad_oracle| for each gradient.
-The SSIM map has no stated bar; it is held to 2e-4 absolute, from the float32
-error of the window sums: E[x'^2] + E[y'^2] (shifted values, at most 0.5)
-summed over 11 + 11 taps carries ~1e-7 absolute rounding error, and S divides
-the variances by sigma11 + sigma22 + C2, which in flat regions is ~C2 = 9e-4:
-|dS| ~ 1e-7 / 9e-4 ~ 1e-4.  (Textured images stay near 1e-6.)
+The SSIM map has no stated bar.  S divides the variances by sigma11 + sigma22
++ C2, which in flat regions is ~C2 = 9e-4, so an absolute error e in the
+float32 window sums E[x'^2] + E[y'^2] moves S by about e / 9e-4.  The 2D kernels
+shift the values of each 11-row band of an 8-column group of windows by one
+pixel of that neighbourhood, so in a flat region the shifted values, and with
+them e, are near zero; a float32 emulation of that arithmetic on the 1080p
+blob render with "same" padding (the worst workload: saturated and dark flat
+regions) gives at most 1e-5.  2D maps are held to 2e-5.  The 3D kernels keep a
+constant shift of 1/2 (shifted values up to 0.5, e ~ 1e-7 over 33 taps, so
+~1e-4 in flat regions): 3D maps are held to 2e-4.
 """
 import numpy as np
 import pytest
@@ -18,7 +23,8 @@ pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
 GRAD_RTOL = 1e-4
-MAP_TOL = 2e-4
+MAP_TOL = 2e-5      # 2D maps
+MAP_TOL_3D = 2e-4   # 3D maps
 
 
 @pytest.fixture(scope="module")
@@ -91,7 +97,8 @@ def _assert_parity(got, ref, want_grad2, label=""):
         assert err <= GRAD_RTOL, f"{label} {k} relative error {err:.3e}"
     if "map" in got and ref.get("map") is not None:
         dmap = np.max(np.abs(got["map"].astype(np.float64) - ref["map"]))
-        assert dmap <= MAP_TOL, f"{label} map off by {dmap:.3e}"
+        tol = MAP_TOL_3D if got["map"].ndim == 5 else MAP_TOL
+        assert dmap <= tol, f"{label} map off by {dmap:.3e}"
 
 
 SMALL_2D = [
@@ -145,11 +152,12 @@ def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
                                   "batch512_valid", "volume128_valid"])
 @pytest.mark.parametrize("path", ["saved", "recompute"])
 def test_parity_workloads(dev, oracle_mod, name, path):
+    """Every workload at full size: means, gradients and the SSIM map."""
     wl = WORKLOADS[name]
     x, y = make_inputs(name)
     dl = dl_vector(name)
-    got = _run(dev, x, y, dl, wl.padding, wl.want_grad2, path)
-    ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2)
+    got = _run(dev, x, y, dl, wl.padding, wl.want_grad2, path, want_map=True)
+    ref = _oracle(oracle_mod, x, y, dl, wl.padding, wl.want_grad2, want_map=True)
     _assert_parity(got, ref, wl.want_grad2, f"{name} {path}")
 
 

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
 GRAD_RTOL = 1e-4
-MAP_TOL = 2e-4
+MAP_TOL = 2e-5
 ETOOLARGE = -6
 
 
