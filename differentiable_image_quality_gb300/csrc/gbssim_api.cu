@@ -280,9 +280,10 @@ Plan2d cached_plan2d(long long planes, int H, int W, int Ho, int Wo, int off, bo
     static Plan2d plans[kSlots];
     static bool used[kSlots] = {};
     static std::mutex m;
-    const PlanKey k{planes, H, W, Ho, Wo, off, grad ? 1 : 0, sm_count, occ, g_seg_rows_override};
+    const int mode = grad ? 1 : 0;
+    const PlanKey k{planes, H, W, Ho, Wo, off, mode, sm_count, occ, g_seg_rows_override};
     const size_t h = (size_t(planes) * 1000003u + size_t(H) * 10007u + size_t(W) * 101u +
-                      size_t(off) * 7u + size_t(grad) * 3u + size_t(occ)) % kSlots;
+                      size_t(off) * 7u + size_t(mode) * 3u + size_t(occ)) % kSlots;
     {
         std::lock_guard<std::mutex> lock(m);
         if (used[h] && keys[h] == k) return plans[h];
@@ -303,6 +304,26 @@ void set_segments(Ssim2dArgs &a, const Plan2d &p, int rows)
     a.seg_base = p.base;
     a.seg_extra = p.extra;
     a.long_blocks = int(p.long_blocks);
+}
+
+// The gradient-mode launch of a 2D call whose arguments are filled in except
+// the segmentation.  With a.partials set, the workspace must hold the plan's
+// partial sums.
+int launch_grad2d(Ssim2dArgs &a, const DeviceInfo *d, int N, bool g2, size_t workspace_bytes,
+                  cudaStream_t s)
+{
+    const long long planes = (long long)N * a.C;
+    a.pair_out = a.vec16 && (reinterpret_cast<uintptr_t>(a.out1) % 8 == 0) &&
+                 (reinterpret_cast<uintptr_t>(a.out2) % 8 == 0);
+    const Plan2d p = cached_plan2d(planes, a.H, a.W, a.Ho, a.Wo, a.off, true, d->sm_count,
+                                   d->occ2d[g2 ? 2 : 1]);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    if (a.partials && workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
+        return GBSSIM_EWORKSPACE;
+    set_segments(a, p, a.H);
+    a.images = N;
+    a.blocks_per_image = int(p.blocks / N);
+    return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), s));
 }
 
 // Upper bound of blocks over every plan (segments never shorter than the minima).
@@ -549,19 +570,12 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
 
     DeviceInfo *d = nullptr;
     if ((rc = device_info(&d))) return rc;
-    const int occ = d->occ2d[grad ? (want_grad2 ? 2 : 1) : 0];
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, grad, d->sm_count, occ);
-    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
-        return GBSSIM_EWORKSPACE;
-
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    set_segments(a, p, grad ? H : Ho);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, grad);
@@ -573,11 +587,18 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     a.counter = static_cast<unsigned *>(workspace);
     a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
     a.mean = out_mean;
+    a.count = double(C) * double(Ho) * double(Wo);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (grad) return launch_grad2d(a, d, N, want_grad2 != 0, workspace_bytes, s);
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, false, d->sm_count,
+                                   d->occ2d[0]);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
+        return GBSSIM_EWORKSPACE;
+    set_segments(a, p, Ho);
     a.images = N;
     a.blocks_per_image = int(p.blocks / N);
-    a.count = double(C) * double(Ho) * double(Wo);
-    return cuda_fail(ssim2d_launch(a, grad, grad && want_grad2, int(p.blocks),
-                                   static_cast<cudaStream_t>(stream)));
+    return cuda_fail(ssim2d_launch(a, false, false, int(p.blocks), s));
 }
 
 int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C, int H, int W,
@@ -622,16 +643,12 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     if (saved_or_null)
         return cuda_fail(scale_fields_launch(f1, f2, grad_img1, grad_img2_or_null, dL, 1.0f,
                                              size_t(C) * H * W, total, d->sm_count, s));
-    const int occ = d->occ2d[g2 ? 2 : 1];
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count, occ);
-    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    set_segments(a, p, H);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, true);
@@ -643,10 +660,8 @@ int ssim_bwd(const float *dL, const float *img1, const float *img2, int N, int C
     a.partials = nullptr;
     a.counter = nullptr;
     a.mean = nullptr;
-    a.images = N;
-    a.blocks_per_image = int(p.blocks / N);
     a.count = double(C) * double(Ho) * double(Wo);
-    return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), s));
+    return launch_grad2d(a, d, N, g2, 0, s);
 }
 
 
@@ -984,17 +999,11 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
     DeviceInfo *d = nullptr;
     if ((rc = device_info(&d))) return rc;
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
-                            d->occ2d[g2 ? 2 : 1]);
-    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
-    if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
-        return GBSSIM_EWORKSPACE;
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    set_segments(a, p, H);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, true);
@@ -1006,10 +1015,8 @@ int ssim_fwd_bwd(const float *img1, const float *img2, int N, int C, int H, int 
     a.counter = static_cast<unsigned *>(workspace);
     a.partials = reinterpret_cast<double *>(static_cast<unsigned char *>(workspace) + kCounterBytes);
     a.mean = out_mean;
-    a.images = N;
-    a.blocks_per_image = int(p.blocks / N);
     a.count = double(C) * double(Ho) * double(Wo);
-    return cuda_fail(ssim2d_launch(a, true, g2, int(p.blocks), static_cast<cudaStream_t>(stream)));
+    return launch_grad2d(a, d, N, g2, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int ssim3d_fwd_bwd(const float *img1, const float *img2, int N, int C, int D, int H, int W,
@@ -1065,9 +1072,10 @@ void gbssim_tune_seg_rows(int rows)
 // waits are made to run out (exercises the bounded-wait failure path).
 void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
 
-// The gradient-mode kernel (with grad2) of ssim_fwd's stored variant, writing
-// besides the two gradient fields of the means (dL = 1) the window statistics
-// and the derivatives of S of every output pixel: stage-by-stage parity.
+// One run of the gradient-mode kernel of ssim_fwd's stored variant with grad2,
+// writing besides the two gradient fields of the means (dL = 1) the window
+// statistics and the derivatives of S of every output pixel: stage-by-stage
+// parity.
 int gbssim_test_stage_dump2d(const float *img1, const float *img2, int N, int C, int H, int W,
                              int padding, float *out_stats, float *out_grads, float *field1,
                              float *field2, void *stream)
@@ -1084,20 +1092,22 @@ int gbssim_test_stage_dump2d(const float *img1, const float *img2, int N, int C,
     if ((rc = device_info(&d))) return rc;
     const int Ho = out_extent(H, padding), Wo = out_extent(W, padding);
     const int off = padding == GBSSIM_VALID ? 0 : kRadius;
-    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
-                                   d->occ2d[2]);
-    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     Ssim2dArgs a{};
     a.x = img1; a.y = img2;
     a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
     a.off = off;
     a.C = C;
-    set_segments(a, p, H);
     a.vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     ssim2d_prepare_staging(a, (long long)N * C, true);
     a.out1 = field1;
     a.out2 = field2;
+    a.pair_out = a.vec16 && (reinterpret_cast<uintptr_t>(a.out1) % 8 == 0) &&
+                 (reinterpret_cast<uintptr_t>(a.out2) % 8 == 0);
+    const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, true, d->sm_count,
+                                   d->occ2d[2]);
+    if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
+    set_segments(a, p, H);
     a.inv_count = float(1.0 / (double(C) * double(Ho) * double(Wo)));
     a.dump_stats = out_stats;
     a.dump_grads = out_grads;

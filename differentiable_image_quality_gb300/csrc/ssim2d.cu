@@ -498,8 +498,9 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             }
         }
         const size_t rowg = plane_off + size_t(q) * a.W;
-        if (a.vec16) {
-            // j0 + KA g is even and W is even: pairs are 8-byte aligned, inside or outside together
+        if (a.pair_out) {
+            // j0 + KA g is even, W % 4 == 0 and the fields are 8-byte aligned: pairs
+            // are 8-byte aligned, inside or outside the image together
 #pragma unroll
             for (int o = 0; o < KA; o += 2) {
                 const int jj = g * KA + o, j = j0 + jj;
@@ -554,17 +555,21 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
 
     // The ring's entries of the previous step were formed at that step's shift;
     // move them to the new one (d = old - new): with x' = x - s_old,
-    //   E[x' + dx] = m1 + dx,  E[(x' + dx)^2] = E[x'^2] + dx (2 m1 + dx),
+    //   E[x' + dx] = m1 + dx,
+    //   E[(x' + dx)^2] + E[(y' + dy)^2] = es + dx (2 m1 + dx) + dy (2 m2 + dy),
     //   E[(x' + dx)(y' + dy)] = e12 + dx (m2 + dy) + dy m1,
-    // exact because every row-pass window's weights sum to one.  Entry 0 is
-    // overwritten by the step's first row before any sum reads it.
+    // exact because every row-pass window's weights sum to one.  The two
+    // corrections of es are summed before es is touched: where the old shift was
+    // far from the rows' values they nearly cancel es, and one rounding of es
+    // plus a term of its size would double the error.  Entry 0 is overwritten by
+    // the step's first row before any sum reads it.
     auto rebase_ring = [&](float2 d) {
 #pragma unroll
         for (int k = 1; k < STEP; ++k) {
             const float2 m = hA[k];
             const float2 v = __fmul2_rn(__ffma2_rn(f2(2.f, 2.f), m, d), d);
             float2 e = hB[k];
-            e.x = (e.x + v.x) + v.y;
+            e.x = e.x + (v.x + v.y);
             e.y = fmaf(d.y, m.x, fmaf(d.x, m.y + d.y, e.y));
             hB[k] = e;
             hA[k] = __fadd2_rn(m, d);

