@@ -186,35 +186,37 @@ struct MomentGrads {
 //   mu = m + sh, sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2,
 //   A1 = 2 mu1 mu2 + C1, A2 = 2 sigma12 + C2, B1 = mu1^2 + mu2^2 + C1,
 //   B2 = sigma_sum + C2.
+// The four factors A1, A2, B1, B2 of S from the shifted moments, each product
+// fused into the sum that uses it (one rounding per term):
+//   B1 = mu1^2 + mu2^2 + C1, B2 = (es + C2) - m1^2 - m2^2,
+//   A1 = 2 mu1 mu2 + C1,     A2 = 2 (e12 - m1 m2) + C2.
+struct SsimTerms {
+    float mu1, mu2, A1, A2, B1, B2;
+};
+
+__device__ __forceinline__ SsimTerms ssim_terms(const Moments &m, float2 sh)
+{
+    SsimTerms t;
+    t.mu1 = m.m1 + sh.x;
+    t.mu2 = m.m2 + sh.y;
+    t.B1 = fmaf(t.mu1, t.mu1, fmaf(t.mu2, t.mu2, kC1));
+    t.B2 = fmaf(-m.m1, m.m1, fmaf(-m.m2, m.m2, m.es + kC2));
+    t.A1 = fmaf(t.mu1 + t.mu1, t.mu2, kC1);
+    t.A2 = fmaf(2.0f, fmaf(-m.m1, m.m2, m.e12), kC2);
+    return t;
+}
+
 __device__ __forceinline__ float ssim_value(const Moments &m, float2 sh)
 {
-    const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, sh);
-    const float2 msq = __fmul2_rn(M, M);
-    const float2 musq = __fmul2_rn(mu, mu);
-    const float ss = m.es - (msq.x + msq.y);
-    const float s12 = fmaf(-m.m1, m.m2, m.e12);
-    const float B1 = (musq.x + musq.y) + kC1;
-    const float B2 = ss + kC2;
-    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
-    const float A2 = fmaf(2.0f, s12, kC2);
-    return (A1 * A2) * rcp_approx(B1 * B2);
+    const SsimTerms t = ssim_terms(m, sh);
+    return (t.A1 * t.A2) * rcp_approx(t.B1 * t.B2);
 }
 
 // The two factors of S: (l, cs) = (A1 / B1, A2 / B2), S = l * cs.
 __device__ __forceinline__ float2 ssim_factors(const Moments &m, float2 sh)
 {
-    const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, sh);
-    const float2 msq = __fmul2_rn(M, M);
-    const float2 musq = __fmul2_rn(mu, mu);
-    const float ss = m.es - (msq.x + msq.y);
-    const float s12 = fmaf(-m.m1, m.m2, m.e12);
-    const float B1 = (musq.x + musq.y) + kC1;
-    const float B2 = ss + kC2;
-    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
-    const float A2 = fmaf(2.0f, s12, kC2);
-    return __fmul2_rn(make_float2(A1, A2), make_float2(rcp_approx(B1), rcp_approx(B2)));
+    const SsimTerms t = ssim_terms(m, sh);
+    return make_float2(t.A1 * rcp_approx(t.B1), t.A2 * rcp_approx(t.B2));
 }
 
 // S and its derivatives with respect to the shifted moments, written as
@@ -230,26 +232,16 @@ template <bool WANT_G2>
 __device__ __forceinline__ float ssim_and_grads(const Moments &m, float2 sh, bool valid,
                                                 MomentGrads &g)
 {
-    const float2 M = make_float2(m.m1, m.m2);
-    const float2 mu = __fadd2_rn(M, sh);
-    const float2 msq = __fmul2_rn(M, M);
-    const float2 musq = __fmul2_rn(mu, mu);
-    const float ss = m.es - (msq.x + msq.y);
-    const float s12 = fmaf(-m.m1, m.m2, m.e12);
-    const float B1 = (musq.x + musq.y) + kC1;
-    const float B2 = ss + kC2;
-    const float A1 = fmaf(mu.x + mu.x, mu.y, kC1);
-    const float A2 = fmaf(2.0f, s12, kC2);
-    const float r1 = rcp_approx(B1), r2 = rcp_approx(B2);
-    const float2 lc = __fmul2_rn(make_float2(A1, A2), make_float2(r1, r2));
-    const float l = valid ? lc.x : 0.0f, cs = valid ? lc.y : 0.0f;
+    const SsimTerms t = ssim_terms(m, sh);
+    const float r1 = rcp_approx(t.B1), r2 = rcp_approx(t.B2);
+    const float l = valid ? t.A1 * r1 : 0.0f, cs = valid ? t.A2 * r2 : 0.0f;
     const float S = l * cs;
     const float lr2 = l * r2;
     g.g_e = -cs * lr2;
     g.g_e12 = lr2 + lr2;
     const float cr1x2 = cs * (r1 + r1);
-    g.g_m1 = fmaf(cr1x2, fmaf(-mu.x, l, mu.y), g.g_e12 * fmaf(m.m1, cs, -m.m2));
-    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-mu.y, l, mu.x), g.g_e12 * fmaf(m.m2, cs, -m.m1));
+    g.g_m1 = fmaf(cr1x2, fmaf(-t.mu1, l, t.mu2), g.g_e12 * fmaf(m.m1, cs, -m.m2));
+    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-t.mu2, l, t.mu1), g.g_e12 * fmaf(m.m2, cs, -m.m1));
     return S;
 }
 

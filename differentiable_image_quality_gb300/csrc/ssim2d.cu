@@ -387,11 +387,12 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             yv[KH + 8] = v.x; yv[KH + 9] = v.y;
         }
         const float2 sh = shift_of(t, g);
-        const float2 nsh = f2(-sh.x, -sh.y);
         float2 accA[KH], accB[KH];  // (m1, m2), (es, e12)
 #pragma unroll
         for (int m = 0; m < KH + 10; ++m) {
-            const float2 p = __fadd2_rn(f2(xv[m], yv[m]), nsh);
+            // two scalar subtractions: x and y come from different loads, and a
+            // packed subtraction would first have to move them into one pair
+            const float2 p = f2(xv[m] - sh.x, yv[m] - sh.y);
             const float2 sq = __fmul2_rn(p, p);
             const float2 q = f2(sq.x + sq.y, p.x * p.y);
 #pragma unroll

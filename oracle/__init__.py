@@ -82,6 +82,8 @@ def _load():
         lib.oracle_ssim3d_grad.argtypes = [dp, dp, dp, i, i, i, i, i, i, dp, dp]
         lib.oracle_ssim3d_grad_at.argtypes = [dp, dp, dp, i, i, i, i, i, i, ctypes.c_longlong,
                                               llp, dp, dp]
+        lib.oracle_ssim3d_map_at.argtypes = [dp, dp, i, i, i, i, i, i, ctypes.c_longlong,
+                                              ctypes.POINTER(ctypes.c_longlong), dp]
         lib.oracle_downscale2x.argtypes = [dp, i, i, dp]
         lib.oracle_ssim2d_components.argtypes = [dp, dp, i, i, i, i, i, dp, dp, dp, dp]
         lib.oracle_ssim_point.argtypes = [ctypes.c_double] * 5 + [dp]
@@ -264,6 +266,20 @@ def ssim3d_grad_at(x, y, dL, padding: str, flat_idx, want_grad2: bool = True):
         idx.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), _ptr(g1), _ptr(g2))
     _check(rc, "ssim3d_grad_at")
     return g1, g2
+
+
+def ssim3d_map_at(x, y, padding: str, flat_idx) -> np.ndarray:
+    """S at the given flat indices of the NCDHW output domain (the map of
+    ssim3d(..., want_map=True) at those places, without forming all of it)."""
+    x, y = _f64(x), _f64(y)
+    N, C, D, H, W = x.shape
+    idx = np.ascontiguousarray(np.asarray(flat_idx, dtype=np.int64))
+    out = np.empty(idx.shape[0])
+    rc = _load().oracle_ssim3d_map_at(
+        _ptr(x), _ptr(y), N, C, D, H, W, _pad(padding), int(idx.shape[0]),
+        idx.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), _ptr(out))
+    _check(rc, "ssim3d_map_at")
+    return out
 
 
 def downscale2x(f) -> np.ndarray:

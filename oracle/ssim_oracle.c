@@ -618,6 +618,41 @@ static void voxel_stats3d(const double *x, const double *y, int D, int H, int W,
     }
 }
 
+/* S at the given output voxels only: idx[t] is a flat index into the NCDHW
+ * output domain [N][C][Do][Ho][Wo]; out[t] = S there, the same direct
+ * 11x11x11 window sums as oracle_ssim3d.  For volumes too large for the whole
+ * map. */
+int oracle_ssim3d_map_at(const double *x, const double *y, int N, int C, int D, int H, int W,
+                         int padding, long long count, const long long *idx, double *out)
+{
+    if (!x || !y || !idx || !out || count < 0 || check3d(N, C, D, H, W, padding)) return -1;
+    const int Do = oracle_out_extent(D, padding), Ho = oracle_out_extent(H, padding),
+              Wo = oracle_out_extent(W, padding);
+    const int off = window_offset(padding);
+    const size_t n = (size_t)D * H * W;
+    const long long m = (long long)Do * Ho * Wo;
+    double w[TAPS];
+    oracle_gauss_window(w);
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (long long t = 0; t < count; ++t) {
+        const long long f = idx[t];
+        if (f < 0 || f >= (long long)N * C * m) {
+            bad = 1;
+            continue;
+        }
+        const size_t pl = (size_t)(f / m);
+        const long long rem = f % m;
+        const int pk = (int)(rem / ((long long)Ho * Wo));
+        const int pi = (int)((rem / Wo) % Ho), pj = (int)(rem % Wo);
+        double st[5];
+        voxel_stats3d(x + pl * n, y + pl * n, D, H, W, off, w, pk, pi, pj, st);
+        out[t] = ssim_point(st[0], st[1], st[2], st[3], st[4], NULL);
+    }
+    return bad ? -1 : 0;
+}
+
 /* 3D counterpart of oracle_ssim2d_grad_at; idx[t] is a flat NCDHW index. */
 int oracle_ssim3d_grad_at(const double *x, const double *y, const double *dL, int N, int C,
                           int D, int H, int W, int padding, long long count,

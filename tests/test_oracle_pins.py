@@ -363,3 +363,21 @@ def test_bad_arguments_rejected(oracle_mod):
         oracle_mod.ssim2d(x, x, "valid")  # H < 11
     with pytest.raises(ValueError):
         oracle_mod.ssim2d(x, x, "reflect")
+
+
+@pytest.mark.parametrize("padding", ["valid", "same"])
+def test_ssim3d_map_at_matches_the_full_map(oracle_mod, padding):
+    """The sampled 3D map (used where the whole map is too large) is the full
+    map's value at each index: both are the direct 1331-term window sums, and
+    the full map is itself pinned above (closed forms, scipy, finite
+    differences of its mean)."""
+    rng = np.random.default_rng(77)
+    x = rng.random((2, 2, 13, 12, 14))
+    y = np.clip(x + rng.normal(0, 0.05, x.shape), 0, 1)
+    _, full = oracle_mod.ssim3d(x, y, padding, want_map=True)
+    idx = rng.integers(0, full.size, size=200)
+    idx[:3] = (0, full.size - 1, full.size // 2)
+    got = oracle_mod.ssim3d_map_at(x, y, padding, idx)
+    np.testing.assert_allclose(got, full.reshape(-1)[idx], rtol=0, atol=1e-14)
+    with pytest.raises(ValueError):
+        oracle_mod.ssim3d_map_at(x, y, padding, [full.size])

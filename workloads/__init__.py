@@ -21,7 +21,12 @@ splat1080_valid    1x3x1080x1920      valid    img1        -1
 splat1080_same     1x3x1080x1920      same     img1, img2  -1
 batch512_valid     8x3x512x512        valid    img1        -1/8
 volume128_valid    1x1x128x128x128    valid    img1        -1
+volume256_valid    1x1x256x256x256    valid    img1        -1
 =================  =================  =======  ==========  ============
+
+volume256_valid is the 128^3 volume's generator at twice the extent: a volume
+whose per-slice intermediate fields (the XY-blurred statistics and the Z
+adjoint of the derivatives, 248 MB each) no longer fit in the GPU's L2.
 """
 from __future__ import annotations
 
@@ -70,6 +75,7 @@ WORKLOADS = {
         Workload("splat1080_same", (1, 3, 1080, 1920), "same", True, -1.0, 1003),
         Workload("batch512_valid", (8, 3, 512, 512), "valid", False, -1.0 / 8.0, 1004),
         Workload("volume128_valid", (1, 1, 128, 128, 128), "valid", False, -1.0, 1005),
+        Workload("volume256_valid", (1, 1, 256, 256, 256), "valid", False, -1.0, 1006),
     )
 }
 
@@ -149,7 +155,7 @@ def make_inputs(name: str):
     elif name == "batch512_valid":
         a = rng.random(wl.shape)
         b = noisy_copy(rng, a, 0.1, gain=0.8, bias=0.1)
-    elif name == "volume128_valid":
+    elif name in ("volume128_valid", "volume256_valid"):
         a = trilinear_noise_volume(rng, *wl.shape)
         b = noisy_copy(rng, a, 0.03)
     else:  # pragma: no cover
