@@ -51,6 +51,7 @@ SIGNATURES = {
 TEST_SIGNATURES = {
     "gbssim_tune_seg_rows": (None, [_i]),
     "gbssim_tune_staging": (None, [_i]),
+    "gbssim_tune_fwd_split": (None, [_i]),
     "gbssim_test_stage_dump2d": (_i, [_fp, _fp, _i, _i, _i, _i, _i, _fp, _fp, _fp, _fp, _vp]),
 }
 

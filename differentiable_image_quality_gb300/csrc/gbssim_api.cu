@@ -29,6 +29,7 @@ struct DeviceInfo {
     int occ2d[3] = {0, 0, 0};  // resident CTAs per SM: forward, gradient, gradient + grad2
     int occ_comp = 0;          // components mode of the forward
     int occ_multi = 0;         // ... several octaves in one launch
+    int occ_fsplit[3] = {0, 0, 0};  // forward split kernels: forward, components, several octaves
     int occ3d[5] = {0, 0, 0, 0, 0};  // 3D: xy; z forward, gradient, + grad2; adjoint
 };
 
@@ -87,6 +88,17 @@ int device_info(DeviceInfo **out)
             if (e != cudaSuccess) return cuda_fail(e);
             if (occ < 1) return cuda_fail(cudaErrorInvalidConfiguration);
             (multi ? d.occ_multi : d.occ_comp) = occ;
+        }
+        for (int kind = 0; kind < 3; ++kind) {
+            const void *k = ssim2d_fsplit_kernel_ptr(kind);
+            const size_t smem = ssim2d_fsplit_smem_bytes();
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(smem));
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_fsplit[kind], k,
+                                                              kThreads2dFsplit, smem);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (d.occ_fsplit[kind] < 1) return cuda_fail(cudaErrorInvalidConfiguration);
         }
         const cudaError_t e3 = ssim3d_prepare(d.occ3d);
         if (e3 != cudaSuccess) return cuda_fail(e3);
@@ -305,6 +317,8 @@ void set_segments(Ssim2dArgs &a, const Plan2d &p, int rows)
     a.seg_extra = p.extra;
     a.long_blocks = int(p.long_blocks);
 }
+
+bool g_fsplit_enabled = true;  // test build: the stream kernel can be forced for the forward
 
 // The gradient-mode launch of a 2D call whose arguments are filled in except
 // the segmentation.  With a.partials set, the workspace must hold the plan's
@@ -590,14 +604,17 @@ int ssim_fwd(const float *img1, const float *img2, int N, int C, int H, int W, i
     a.count = double(C) * double(Ho) * double(Wo);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (grad) return launch_grad2d(a, d, N, want_grad2 != 0, workspace_bytes, s);
+    // forward only: the split kernel where the inputs are staged by tensor copies
+    const bool fs = a.tma && g_fsplit_enabled;
     const Plan2d p = cached_plan2d((long long)N * C, H, W, Ho, Wo, off, false, d->sm_count,
-                                   d->occ2d[0]);
+                                   fs ? d->occ_fsplit[0] : d->occ2d[0]);
     if (p.blocks > INT_MAX) return GBSSIM_ESHAPE;
     if (workspace_bytes < kCounterBytes + size_t(p.blocks) * sizeof(double))
         return GBSSIM_EWORKSPACE;
     set_segments(a, p, Ho);
     a.images = N;
     a.blocks_per_image = int(p.blocks / N);
+    if (fs) return cuda_fail(ssim2d_fsplit_launch(a, false, int(p.blocks), s, false));
     return cuda_fail(ssim2d_launch(a, false, false, int(p.blocks), s));
 }
 
@@ -746,11 +763,19 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
         blocks = p.blocks;
         return GBSSIM_OK;
     };
+    // the forward split kernel where every octave's images allow tensor copies
+    // (16-byte aligned, W_o % 4 == 0; the downscaled ones are 256-byte aligned)
+    bool fs = g_fsplit_enabled && staging_mode() != 1 &&
+              (reinterpret_cast<uintptr_t>(img1) % 16 == 0) &&
+              (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
+    for (int o = 0; o < octaves; ++o) fs = fs && (L.W[o] % 4 == 0);
     cudaError_t e;
     if (octaves == 1) {
         Ssim2dArgs a0;
         long long b0 = 0;
-        if ((rc = octave_args(0, partials, 0, d->occ_comp, 0, a0, b0))) return rc;
+        if ((rc = octave_args(0, partials, 0, fs ? d->occ_fsplit[1] : d->occ_comp, 0, a0, b0)))
+            return rc;
+        if (fs && a0.tma) return cuda_fail(ssim2d_fsplit_launch(a0, true, int(b0), s, false));
         return cuda_fail(ssim2d_components_launch(a0, int(b0), s, false));
     }
     // the downscaled octaves first, up to kChainLevels per launch (each waits
@@ -791,9 +816,9 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
             long long blocks = 0;
             const double share = double(out_extent(L.H[o0 + k], padding)) *
                                  out_extent(L.W[o0 + k], padding) / work;
-            const long long target =
-                std::max(1LL, (long long)(share * d->sm_count * d->occ_multi + 0.5));
-            if ((rc = octave_args(o0 + k, part, map_pos, d->occ_multi, target, m.oct[k], blocks)))
+            const int occ = fs ? d->occ_fsplit[2] : d->occ_multi;
+            const long long target = std::max(1LL, (long long)(share * d->sm_count * occ + 0.5));
+            if ((rc = octave_args(o0 + k, part, map_pos, occ, target, m.oct[k], blocks)))
                 return rc;
             // octave 0 reads the caller's images: its blocks need not wait for the
             // octave chain ahead (which itself waited for the work before it)
@@ -805,7 +830,10 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
             map_pos += 3 * m.oct[k].map_stride;
         }
         m.first[m.count] = int(total);
-        if ((e = ssim2d_components_multi_launch(m, s)) != cudaSuccess) return cuda_fail(e);
+        bool all_tma = fs;
+        for (int k = 0; k < m.count; ++k) all_tma = all_tma && m.oct[k].tma;
+        e = all_tma ? ssim2d_fsplit_multi_launch(m, s) : ssim2d_components_multi_launch(m, s);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return GBSSIM_OK;
 }
@@ -1071,6 +1099,11 @@ void gbssim_tune_seg_rows(int rows)
 // them (the product behaviour), 1 cp.async copies only, 2 tensor copies whose
 // waits are made to run out (exercises the bounded-wait failure path).
 void gbssim_tune_staging(int mode) { ssim2d_set_staging_mode(mode); }
+
+// Force the stream kernel for every later forward-only and per-octave launch
+// (on = 0), or let the forward split kernel run where it applies (on = 1, the
+// product behaviour).
+void gbssim_tune_fwd_split(int on) { g_fsplit_enabled = on != 0; }
 
 // One run of the gradient-mode kernel of ssim_fwd's stored variant with grad2,
 // writing besides the two gradient fields of the means (dL = 1) the window

@@ -21,6 +21,11 @@ void gbssim_tune_seg_rows(int rows);
  * staging wait runs out (the failure path: NaN means, the device status bit). */
 void gbssim_tune_staging(int mode);
 
+/* Force the stream kernel for every later forward-only and per-octave launch
+ * in the process (on = 0), or let the forward split kernel run where the
+ * inputs allow tensor copies (on = 1, the default). */
+void gbssim_tune_fwd_split(int on);
+
 /* Stage-by-stage parity of the 2D gradient kernel: one run of the kernel of
  * ssim_fwd's stored variant with grad2 on img1 / img2 ([N, C, H, W] float32,
  * device) that also writes, for every output pixel of [N, C, Ho, Wo]:

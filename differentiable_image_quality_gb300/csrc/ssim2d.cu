@@ -209,7 +209,10 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
 {
     static_assert(!(COMP && GRAD), "components mode is forward only");
     static_assert(!DUMP || (GRAD && G2), "the statistics dump runs in gradient mode with grad2");
-    constexpr int KH = GRAD ? 8 : 4;   // columns per row-pass work item
+    // columns per row-pass work item: an item forms the shifted products of its
+    // KH + 10 input columns once, so wider items repeat fewer of them (8: each
+    // input's products are formed 2.25 times; 4: 3.5 times)
+    constexpr int KH = 8;
     constexpr int NGH = SW / KH;
     static_assert(SW % KH == 0, "strip width must be a multiple of the row-pass block");
 
@@ -773,6 +776,295 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
     }
 }
 
+// ------------------------------------------------- forward-only split kernel
+//
+// The forward-only walk (mean and map; components mode: l, cs and S) with the
+// two phases of a step on the two warpgroups of a 256-thread CTA, which run at
+// the same time:
+//   warpgroup 0 (V, one thread per statistic column): the column pass of step
+//     t -- the statistic ring, SSIM (or l and cs), the sums and the maps;
+//   warpgroup 1 (W): the row pass of step t+1; one of its threads issues the
+//     tensor copies, all of them wait for the copies they read.
+// One CTA barrier per step; the row-pass results (hb) and the shifts are
+// double-buffered across it.  The column pass is a chain of dependent window
+// sums and SSIM terms per row, the row pass many independent sums: run side by
+// side they fill each other's idle issue slots, where the stream kernel runs
+// them one after the other between barriers.  Needs tensor-copy staging (a.tma).
+constexpr int NTF = 2 * NT;                                   // threads of a CTA
+constexpr size_t kFInBytes = size_t(2) * NBUF * XB * sizeof(float);
+constexpr size_t kFSplitSmem = 128 + kFInBytes + 2 * kHbBytes;  // + alignment slack
+constexpr int kFSplitBlocks = 3;                              // resident CTAs per SM
+static_assert(kFSplitBlocks * (kFSplitSmem + 1024 + 512) <= 233472,
+              "three forward split CTAs fit in an SM's shared memory");
+
+template <bool COMP, bool MULTI>
+__device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
+{
+    constexpr int KH = 8;  // columns per row-pass work item
+    constexpr int NGH = SW / KH;
+    extern __shared__ __align__(128) unsigned char smem_fs[];
+    unsigned char *base = smem_fs + ((128 - (smem_u32(smem_fs) & 127)) & 127);
+    float *xs = reinterpret_cast<float *>(base);   // [2][XB], tensor-copy destinations
+    float *ys = xs + NBUF * XB;                    // [2][XB]
+    float4 *hbuf = reinterpret_cast<float4 *>(base + kFInBytes);  // [2][HBUF]
+    __shared__ double red[COMP ? 3 : 1][NTF / 32];
+    __shared__ uint64_t bars[2];
+    __shared__ float2 shifts[2][NGH];
+
+    pdl_trigger();
+    if (!a.no_wait) pdl_wait();
+    const int tid = threadIdx.x;
+    const SegWork w = segment_of(a, block);
+    const int plane = w.plane;
+    // geometry of the forward walk (as in stream_body): input row r completes
+    // statistic row p = r + off - 10
+    const int sc0 = w.strip * SW - stat_shift(a.off);
+    const int ic0 = sc0 - a.off;
+    const int R0 = w.r0 - a.off;
+    const int nrows = w.r1 - w.r0 + 10;
+    const int steps = (nrows + STEP - 1) / STEP;
+    const int Rend = R0 + nrows;
+    const int nstat = max(0, min(SW, a.Wo - sc0));
+    const int ngh = min(NGH, (nstat + KH - 1) / KH);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init_fence();
+    }
+    if (ngh < NGH) {  // columns no item writes read as zeros
+        constexpr int n4 = int(2 * kHbBytes / 16);
+        for (int i = tid; i < n4; i += NTF) hbuf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < 2 * NGH) shifts[tid / NGH][tid % NGH] = f2(0.f, 0.f);
+    __syncthreads();
+
+    bool failed = false;
+    float ssum = 0.0f, lsum = 0.0f, csum = 0.0f;
+    if (tid < NT) {
+        // ================================================================ V
+        float2 hA[STEP], hB[STEP];
+#pragma unroll
+        for (int k = 0; k < STEP; ++k) hA[k] = hB[k] = f2(0.f, 0.f);
+        const int pc = sc0 + tid;
+        const bool col_ok = (pc >= 0) && (pc < a.Wo);
+        const bool v_warp = (tid & ~31) < nstat;
+        float2 sh = f2(0.f, 0.f);
+        int klo = 0, khi = 0;
+        const float4 *hb = hbuf;
+        auto v_row = [&](auto K_, int t) {
+            constexpr int k = decltype(K_)::value;
+            const float4 h = hb[k * RP + tid];
+            hA[k] = lo(h);
+            hB[k] = hi(h);
+            if (k < klo) return;  // warm-up row: only the ring entries are needed
+            const bool ok = col_ok && (k < khi);
+            const int p = R0 + t * STEP + k + a.off - 10;
+            const float2 M = ring_sum2<k>(hA);
+            const float2 E = ring_sum2<k>(hB);
+            const Moments mo{M.x, M.y, E.x, E.y};
+            if (COMP) {
+                const float2 lc = ssim_factors(mo, sh);
+                const float S = lc.x * lc.y;
+                lsum += ok ? lc.x : 0.0f;
+                csum += ok ? lc.y : 0.0f;
+                ssum += ok ? S : 0.0f;
+                if (a.map && ok) {
+                    float *m = a.map + (size_t(plane) * a.Ho + p) * a.Wo + pc;
+                    m[0] = lc.x;
+                    m[a.map_stride] = lc.y;
+                    m[2 * a.map_stride] = S;
+                }
+            } else {
+                const float S = ssim_value(mo, sh);
+                ssum += ok ? S : 0.0f;
+                if (a.map && ok) a.map[(size_t(plane) * a.Ho + p) * a.Wo + pc] = S;
+            }
+        };
+        failed = __syncthreads_or(0);  // H(0) is in hb[0]
+        for (int t = 0; t < steps && !failed; ++t) {
+            if (v_warp) {
+                const int rb = R0 + t * STEP;
+                const int pb = rb + a.off - 10;
+                klo = max(max(0, R0 + 10 - rb), -pb);
+                khi = min(min(STEP, Rend - rb), a.Ho - pb);
+                hb = hbuf + (t & 1) * (kHbBytes / 16);
+                const float2 nsh = shifts[t & 1][tid / KH];
+                if (t > 0) {
+                    // the ring's entries of step t-1 to this step's shift (see stream_body)
+                    const float2 d = f2(sh.x - nsh.x, sh.y - nsh.y);
+#pragma unroll
+                    for (int k = 1; k < STEP; ++k) {
+                        const float2 m = hA[k];
+                        const float2 v = __fmul2_rn(__ffma2_rn(f2(2.f, 2.f), m, d), d);
+                        float2 e = hB[k];
+                        e.x = e.x + (v.x + v.y);
+                        e.y = fmaf(d.y, m.x, fmaf(d.x, m.y + d.y, e.y));
+                        hB[k] = e;
+                        hA[k] = __fadd2_rn(m, d);
+                    }
+                }
+                sh = nsh;
+                v_row(std::integral_constant<int, 0>{}, t);
+                v_row(std::integral_constant<int, 1>{}, t);
+                v_row(std::integral_constant<int, 2>{}, t);
+                v_row(std::integral_constant<int, 3>{}, t);
+                v_row(std::integral_constant<int, 4>{}, t);
+                v_row(std::integral_constant<int, 5>{}, t);
+                v_row(std::integral_constant<int, 6>{}, t);
+                v_row(std::integral_constant<int, 7>{}, t);
+                v_row(std::integral_constant<int, 8>{}, t);
+                v_row(std::integral_constant<int, 9>{}, t);
+                v_row(std::integral_constant<int, 10>{}, t);
+            }
+            if (__syncthreads_or(0)) {
+                failed = true;
+                break;
+            }
+        }
+    } else {
+        // ================================================================ W
+        const int wt = tid - NT;
+        int issued = 0;
+        auto load_block = [&](int t) {  // block t into buffer t % 2 (thread wt == 0)
+            mbar_arrive_expect_tx(&bars[t & 1], kBlockTx + a.tx_extra);
+            tma_load_3d(xs + (t & 1) * XB, &a.tm_x, ic0, R0 + t * STEP, plane, &bars[t & 1]);
+            tma_load_3d(ys + (t & 1) * XB, &a.tm_y, ic0, R0 + t * STEP, plane, &bars[t & 1]);
+            ++issued;
+        };
+        // the shift of group g for block t (see stream_body's shift_of)
+        auto shift_of = [&](int t, int g) -> float2 {
+            const int rb = R0 + t * STEP;
+            const int kk = min(max(rb, 0), a.H - 1) - rb;
+            if (kk < 0 || kk >= STEP) return f2(0.f, 0.f);
+            const int cc = min(max(ic0 + g * KH + (KH + 9) / 2, 0), a.W - 1) - ic0;
+            const int i = (t & 1) * XB + kk * IWP + cc;
+            return f2(fminf(fmaxf(xs[i], 0.f), 1.f), fminf(fmaxf(ys[i], 0.f), 1.f));
+        };
+        auto h_item = [&](int t, int item) {
+            const int g = item / STEP, k = item - g * STEP;
+            const int base_i = (t & 1) * XB + k * IWP + g * KH;
+            float xv[KH + 10], yv[KH + 10];
+#pragma unroll
+            for (int m = 0; m < KH + 8; m += 4) {
+                const float4 u = *reinterpret_cast<const float4 *>(xs + base_i + m);
+                const float4 v = *reinterpret_cast<const float4 *>(ys + base_i + m);
+                xv[m] = u.x; xv[m + 1] = u.y; xv[m + 2] = u.z; xv[m + 3] = u.w;
+                yv[m] = v.x; yv[m + 1] = v.y; yv[m + 2] = v.z; yv[m + 3] = v.w;
+            }
+            {
+                const float2 u = *reinterpret_cast<const float2 *>(xs + base_i + KH + 8);
+                const float2 v = *reinterpret_cast<const float2 *>(ys + base_i + KH + 8);
+                xv[KH + 8] = u.x; xv[KH + 9] = u.y;
+                yv[KH + 8] = v.x; yv[KH + 9] = v.y;
+            }
+            const float2 sh = shift_of(t, g);
+            if (k == 0) shifts[t & 1][g] = sh;
+            float2 accA[KH], accB[KH];
+#pragma unroll
+            for (int m = 0; m < KH + 10; ++m) {
+                const float2 p = f2(xv[m] - sh.x, yv[m] - sh.y);
+                const float2 sq = __fmul2_rn(p, p);
+                const float2 q = f2(sq.x + sq.y, p.x * p.y);
+#pragma unroll
+                for (int o = 0; o < KH; ++o) {
+                    const int b = m - o;
+                    if (b < 0 || b > 10) continue;
+                    const float2 wt2 = splat(tap(b));
+                    if (b == 0) {
+                        accA[o] = __fmul2_rn(wt2, p);
+                        accB[o] = __fmul2_rn(wt2, q);
+                    } else {
+                        accA[o] = __ffma2_rn(wt2, p, accA[o]);
+                        accB[o] = __ffma2_rn(wt2, q, accB[o]);
+                    }
+                }
+            }
+            float4 *dst = hbuf + (t & 1) * (kHbBytes / 16) + k * RP + g * KH;
+#pragma unroll
+            for (int o = 0; o < KH; ++o)
+                dst[o] = make_float4(accA[o].x, accA[o].y, accB[o].x, accB[o].y);
+        };
+
+        if (wt == 0) {
+            load_block(0);
+            if (steps > 1) load_block(1);
+        }
+        const int nh_items = STEP * ngh;
+        bool ok = mbar_wait_bounded(&bars[0], 0, kWaitCycles);
+        if (ok)
+            for (int i = wt; i < nh_items; i += NT) h_item(0, i);
+        failed = __syncthreads_or(!ok);  // H(0) is in hb[0]
+        for (int t = 0; t < steps && !failed; ++t) {
+            // block t + 2 goes into the buffer H(t) read in the last step
+            if (ok && wt == 0 && t + 2 < steps) load_block(t + 2);
+            if (ok && t + 1 < steps) {
+                ok = mbar_wait_bounded(&bars[(t + 1) & 1], ((t + 1) >> 1) & 1, kWaitCycles);
+                if (ok)
+                    for (int i = wt; i < nh_items; i += NT) h_item(t + 1, i);
+            }
+            if (__syncthreads_or(!ok)) {
+                failed = true;
+                break;
+            }
+        }
+        if (failed && wt == 0) {
+            // let the tensor copies in flight land (bounded), then record the failure
+            const long long t0 = clock64();
+            for (int b = 0; b < 2; ++b) {
+                const int cnt = (issued + 1 - b) / 2;
+                const long long left = kDrainCycles - (clock64() - t0);
+                if (cnt > 0 && left > 0) mbar_wait_bounded(&bars[b], (cnt - 1) & 1, left);
+            }
+            atomicOr(&g_staging_status, 1u);
+        }
+    }
+
+    if (a.partials != nullptr) {
+        const double nan = __longlong_as_double(0x7ff8000000000000LL);
+        if (COMP) {
+            const double tl = block_sum<NTF>(lsum, red[0]);
+            const double tc = block_sum<NTF>(csum, red[1]);
+            const double ts = block_sum<NTF>(ssum, red[2]);
+            if (tid == 0) {
+                a.partials[w.slot] = failed ? nan : tl;
+                a.partials[a.segments + w.slot] = failed ? nan : tc;
+                a.partials[2 * a.segments + w.slot] = failed ? nan : ts;
+            }
+            if (!MULTI)
+                finish_means_k<NTF, 3>(a.partials, a.segments, a.counter, a.mean, a.images,
+                                       a.blocks_per_image, a.count);
+        } else {
+            const double tot = block_sum<NTF>(ssum, red[0]);
+            if (tid == 0) a.partials[w.slot] = failed ? nan : tot;
+            finish_means<NTF>(a.partials, a.counter, a.mean, a.images, a.blocks_per_image, a.count);
+        }
+    }
+}
+
+template <bool COMP>
+__global__ void __launch_bounds__(NTF, kFSplitBlocks)
+    ssim2d_fsplit_kernel(const __grid_constant__ Ssim2dArgs a)
+{
+    fsplit_body<COMP, false>(a, blockIdx.x);
+}
+
+// Components mode for several octaves in one launch (see the stream kernel's).
+__global__ void __launch_bounds__(NTF, kFSplitBlocks)
+    ssim2d_fsplit_multi_kernel(const __grid_constant__ Ssim2dMulti m)
+{
+    int o = 0;
+    while (o + 1 < m.count && int(blockIdx.x) >= m.first[o + 1]) ++o;
+    fsplit_body<true, true>(m.oct[o], int(blockIdx.x) - m.first[o]);
+    if (!finish_ticket<NTF>(m.counter)) return;
+    for (int k = 0; k < m.count; ++k) {
+        const Ssim2dArgs &q = m.oct[k];
+        reduce_means_k<NTF, 3>(q.partials, q.segments, q.mean, q.images, q.blocks_per_image,
+                               q.count);
+    }
+    if (threadIdx.x == 0) *m.counter = 0u;
+}
+
 template <bool GRAD, bool G2, bool COMP = false>
 __global__ void __launch_bounds__(NT, min_blocks<GRAD, G2>())
     ssim2d_stream_kernel(const __grid_constant__ Ssim2dArgs a)
@@ -1158,6 +1450,47 @@ cudaError_t ssim2d_dump_launch(const Ssim2dArgs &a, int blocks, cudaStream_t s)
     return cudaGetLastError();
 }
 #endif
+
+size_t ssim2d_fsplit_smem_bytes() { return kFSplitSmem; }
+
+const void *ssim2d_fsplit_kernel_ptr(int kind)
+{
+    if (kind == 0) return reinterpret_cast<const void *>(ssim2d_fsplit_kernel<false>);
+    if (kind == 1) return reinterpret_cast<const void *>(ssim2d_fsplit_kernel<true>);
+    return reinterpret_cast<const void *>(ssim2d_fsplit_multi_kernel);
+}
+
+cudaError_t ssim2d_fsplit_launch(const Ssim2dArgs &a, bool comp, int blocks, cudaStream_t s,
+                                 bool early)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(NTF);
+    cfg.dynamicSmemBytes = kFSplitSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return comp ? cudaLaunchKernelEx(&cfg, ssim2d_fsplit_kernel<true>, a)
+                : cudaLaunchKernelEx(&cfg, ssim2d_fsplit_kernel<false>, a);
+}
+
+cudaError_t ssim2d_fsplit_multi_launch(const Ssim2dMulti &m, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(m.first[m.count]));
+    cfg.blockDim = dim3(NTF);
+    cfg.dynamicSmemBytes = kFSplitSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ssim2d_fsplit_multi_kernel, m);
+}
 
 cudaError_t ssim2d_launch(const Ssim2dArgs &a, bool grad, bool g2, int blocks, cudaStream_t s)
 {

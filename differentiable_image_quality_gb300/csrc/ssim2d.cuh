@@ -91,6 +91,17 @@ struct Ssim2dMulti {
 cudaError_t ssim2d_components_multi_launch(const Ssim2dMulti &m, cudaStream_t s);
 const void *ssim2d_components_multi_kernel_ptr();
 
+// The forward-only walk split between two warpgroups of a 256-thread CTA (the
+// column pass of step t beside the row pass of step t+1); needs a.tma.  kind:
+// 0 forward (mean, map), 1 components mode, 2 several octaves in components
+// mode.  Same plans and results as the stream kernel's forward modes.
+constexpr int kThreads2dFsplit = 256;
+size_t ssim2d_fsplit_smem_bytes();
+const void *ssim2d_fsplit_kernel_ptr(int kind);
+cudaError_t ssim2d_fsplit_launch(const Ssim2dArgs &a, bool comp, int blocks, cudaStream_t s,
+                                 bool early);
+cudaError_t ssim2d_fsplit_multi_launch(const Ssim2dMulti &m, cudaStream_t s);
+
 // Octaves lo + 1 .. lo + levels (levels <= kChainLevels) of both images from
 // octave lo in one launch: 2x2 box means, ragged edges over in-range pixels.
 // Launched early; with wait_first the kernel ahead wrote octave lo, otherwise

@@ -148,6 +148,48 @@ def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
             lib.gbssim_tune_seg_rows(0)
 
 
+@pytest.mark.parametrize("shape,padding,seed", [
+    ((1, 3, 64, 64), "valid", 31), ((2, 2, 37, 300), "same", 32), ((1, 1, 250, 256), "valid", 33),
+    ((1, 2, 130, 236), "same", 34), ((1, 1, 11, 12), "valid", 35)])
+def test_forward_kernels_agree(dev, oracle_mod, shape, padding, seed):
+    """Forward only and the per-octave stage on images staged by tensor copies
+    run the split forward kernel; the test build can force the stream kernel
+    there.  Both must match the oracle."""
+    import torch
+
+    import differentiable_image_quality_gb300 as pkg
+    from differentiable_image_quality_gb300 import _abi
+
+    x, y = uniform_pair(shape, 500 + seed, std=0.08)
+    N = shape[0]
+    ref_mean, ref_map = oracle_mod.ssim2d(x, y, padding, want_map=True)
+    octs = 1
+    while octs < 3 and min(pkg.pyramid_extents(shape[2], shape[3], octs + 1)[-1]) >= (
+            11 if padding == "valid" else 1):
+        octs += 1
+    ref_pm, ref_pmaps = oracle_mod.ssim2d_pyramid(x, y, padding, octs, want_maps=True)
+    tx, ty = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+    with _abi.using_test_library() as lib:
+        for split in (1, 0):
+            lib.gbssim_tune_fwd_split(split)
+            try:
+                mean = torch.full((N,), float("nan"), device=dev)
+                ho, wo = ref_map.shape[2:]
+                smap = torch.full((N, shape[1], ho, wo), float("nan"), device=dev)
+                pkg.ssim_fwd(tx, ty, padding, mean, out_map=smap)
+                pm, pmaps = pkg.ssim_pyramid(tx, ty, padding, octs, want_maps=True)
+                torch.cuda.synchronize()
+            finally:
+                lib.gbssim_tune_fwd_split(1)
+            label = f"split={split} {shape} {padding}"
+            assert np.max(np.abs(mean.cpu().numpy() - ref_mean)) <= MEAN_TOL, label
+            assert np.max(np.abs(smap.cpu().numpy() - ref_map)) <= MAP_TOL, label
+            assert np.max(np.abs(pm.cpu().numpy() - ref_pm)) <= MEAN_TOL, label
+            for o in range(octs):
+                tol = MAP_TOL if o == 0 else 1e-4
+                assert np.max(np.abs(pmaps[o].cpu().numpy() - ref_pmaps[o])) <= tol, (label, o)
+
+
 @pytest.mark.parametrize("name", ["tiny64_valid", "splat1080_valid", "splat1080_same",
                                   "batch512_valid", "volume128_valid"])
 @pytest.mark.parametrize("path", ["saved", "recompute"])
