@@ -66,6 +66,10 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the extra timed variants")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name from workloads.WORKLOADS (default: the 1080p valid pair)")
+    ap.add_argument("--path", choices=["train", "infer", "pyramid"], default="train",
+                    help="the call a step times: train (training forward + stored backward, the "
+                         "metric), infer (forward only) or pyramid (the six-octave per-octave "
+                         "stage, 2D only); the last two print a short line (for profiling)")
     return ap.parse_args()
 
 
@@ -403,6 +407,38 @@ def workload_summary(w, timed, steps, peaks, alu_peak_tflops):
             "hbm_frac": rf["hbm_frac"], "alu_frac": rf["alu_frac"], "steps": steps}
 
 
+def run_path(args, pkg, torch, dev, w, timed, world, rank):
+    """One call timed on its own (forward only, or the per-octave stage)."""
+    x, wl, mp = w["x"], w["wl"], w["mp"]
+    if args.path == "infer":
+        fn, what = w["fwd_infer"], "forward only (inference), mean of each image"
+    else:
+        if w["is3d"]:
+            raise SystemExit("--path pyramid needs a 2D workload")
+        octs = 6
+        means = torch.empty((octs, 3, x.shape[0]), device=dev)
+        tx, ty = w["tx"], w["ty"]
+
+        def fn():
+            pkg.ssim_pyramid(tx, ty, wl.padding, octs, out_means=means)
+
+        what = f"per-octave stage, {octs} octaves (l, cs, S means)"
+    ts, _ = timed(fn, None, args.steps, max(3, args.warmup))
+    total_ms = max_over_ranks(sum(ts), world, dev)
+    if rank == 0:
+        unit = UNIT if not w["is3d"] else "Mvoxel/s"
+        print(json.dumps({"metric": f"fp32 SSIM {what}, {unit}", "path": args.path,
+                          "value": whole_job_rate(mp, world, args.steps, total_ms), "unit": unit,
+                          "n_gpus": world, "steps": args.steps, "ms_per_step": total_ms / args.steps,
+                          "higher_is_better": True,
+                          "config": {"workload": args.workload, "shape": list(x.shape),
+                                     "padding": wl.padding}}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -431,6 +467,9 @@ def run_ours(args):
     def train_step():
         w["fwd_train"]()
         w["bwd_saved"]()
+
+    if args.path != "train":
+        return run_path(args, pkg, torch, dev, w, timed, world, rank)
 
     # the step as a whole (no event between forward and backward, so the
     # backward's launch may overlap the forward's tail), then the two halves
