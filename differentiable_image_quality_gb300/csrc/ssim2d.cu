@@ -802,6 +802,8 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
 {
     constexpr int KH = 8;  // columns per row-pass work item
     constexpr int NGH = SW / KH;
+    static_assert(STEP * NGH >= NT && 2 * (STEP * NGH - NT) <= NT,
+                  "a step's row pass is one item per thread plus at most one half item");
     extern __shared__ __align__(128) unsigned char smem_fs[];
     unsigned char *base = smem_fs + ((128 - (smem_u32(smem_fs) & 127)) & 127);
     float *xs = reinterpret_cast<float *>(base);   // [2][XB], tensor-copy destinations
@@ -941,33 +943,35 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
             const int i = (t & 1) * XB + kk * IWP + cc;
             return f2(fminf(fmaxf(xs[i], 0.f), 1.f), fminf(fmaxf(ys[i], 0.f), 1.f));
         };
-        auto h_item = [&](int t, int item) {
-            const int g = item / STEP, k = item - g * STEP;
-            const int base_i = (t & 1) * XB + k * IWP + g * KH;
-            float xv[KH + 10], yv[KH + 10];
+        // the row pass of KW columns from column c0 (a multiple of 4) of group g,
+        // row k of block t
+        auto h_cols = [&](auto KW_, int t, int g, int k, int c0) {
+            constexpr int KW = decltype(KW_)::value;
+            const int base_i = (t & 1) * XB + k * IWP + c0;
+            float xv[KW + 10], yv[KW + 10];
 #pragma unroll
-            for (int m = 0; m < KH + 8; m += 4) {
+            for (int m = 0; m < KW + 8; m += 4) {
                 const float4 u = *reinterpret_cast<const float4 *>(xs + base_i + m);
                 const float4 v = *reinterpret_cast<const float4 *>(ys + base_i + m);
                 xv[m] = u.x; xv[m + 1] = u.y; xv[m + 2] = u.z; xv[m + 3] = u.w;
                 yv[m] = v.x; yv[m + 1] = v.y; yv[m + 2] = v.z; yv[m + 3] = v.w;
             }
             {
-                const float2 u = *reinterpret_cast<const float2 *>(xs + base_i + KH + 8);
-                const float2 v = *reinterpret_cast<const float2 *>(ys + base_i + KH + 8);
-                xv[KH + 8] = u.x; xv[KH + 9] = u.y;
-                yv[KH + 8] = v.x; yv[KH + 9] = v.y;
+                const float2 u = *reinterpret_cast<const float2 *>(xs + base_i + KW + 8);
+                const float2 v = *reinterpret_cast<const float2 *>(ys + base_i + KW + 8);
+                xv[KW + 8] = u.x; xv[KW + 9] = u.y;
+                yv[KW + 8] = v.x; yv[KW + 9] = v.y;
             }
             const float2 sh = shift_of(t, g);
-            if (k == 0) shifts[t & 1][g] = sh;
-            float2 accA[KH], accB[KH];
+            if (k == 0 && c0 == g * KH) shifts[t & 1][g] = sh;
+            float2 accA[KW], accB[KW];
 #pragma unroll
-            for (int m = 0; m < KH + 10; ++m) {
+            for (int m = 0; m < KW + 10; ++m) {
                 const float2 p = f2(xv[m] - sh.x, yv[m] - sh.y);
                 const float2 sq = __fmul2_rn(p, p);
                 const float2 q = f2(sq.x + sq.y, p.x * p.y);
 #pragma unroll
-                for (int o = 0; o < KH; ++o) {
+                for (int o = 0; o < KW; ++o) {
                     const int b = m - o;
                     if (b < 0 || b > 10) continue;
                     const float2 wt2 = splat(tap(b));
@@ -980,28 +984,47 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
                     }
                 }
             }
-            float4 *dst = hbuf + (t & 1) * (kHbBytes / 16) + k * RP + g * KH;
+            float4 *dst = hbuf + (t & 1) * (kHbBytes / 16) + k * RP + c0;
 #pragma unroll
-            for (int o = 0; o < KH; ++o)
+            for (int o = 0; o < KW; ++o)
                 dst[o] = make_float4(accA[o].x, accA[o].y, accB[o].x, accB[o].y);
+        };
+        // The row pass of block t: items of KH columns x 1 row, one per thread;
+        // the items beyond the warpgroup's threads are done as two half items
+        // each (4 columns), by threads that rotate with the step and the block,
+        // so that the warps' shares of a step differ by half an item at most
+        // and no scheduler partition holds the extra work every step.
+        auto h_block = [&](int t) {
+            const int n_items = STEP * ngh;
+            if (wt < n_items) {
+                const int g = wt / STEP;
+                h_cols(std::integral_constant<int, KH>{}, t, g, wt - g * STEP, g * KH);
+            }
+            const int n_half = 2 * (n_items - NT);
+            if (n_half > 0) {
+                const int j = (wt + 32 * ((t + block) & 3)) & (NT - 1);
+                if (j < n_half) {
+                    const int item = NT + (j >> 1);
+                    const int g = item / STEP;
+                    h_cols(std::integral_constant<int, KH / 2>{}, t, g, item - g * STEP,
+                           g * KH + (j & 1) * (KH / 2));
+                }
+            }
         };
 
         if (wt == 0) {
             load_block(0);
             if (steps > 1) load_block(1);
         }
-        const int nh_items = STEP * ngh;
         bool ok = mbar_wait_bounded(&bars[0], 0, kWaitCycles);
-        if (ok)
-            for (int i = wt; i < nh_items; i += NT) h_item(0, i);
+        if (ok) h_block(0);
         failed = __syncthreads_or(!ok);  // H(0) is in hb[0]
         for (int t = 0; t < steps && !failed; ++t) {
             // block t + 2 goes into the buffer H(t) read in the last step
             if (ok && wt == 0 && t + 2 < steps) load_block(t + 2);
             if (ok && t + 1 < steps) {
                 ok = mbar_wait_bounded(&bars[(t + 1) & 1], ((t + 1) >> 1) & 1, kWaitCycles);
-                if (ok)
-                    for (int i = wt; i < nh_items; i += NT) h_item(t + 1, i);
+                if (ok) h_block(t + 1);
             }
             if (__syncthreads_or(!ok)) {
                 failed = true;
