@@ -1014,9 +1014,11 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
 
         if (wt == 0) {
             load_block(0);
-            if (steps > 1) load_block(1);
         }
+        // block 1 goes out once block 0 has landed: issued together, the grid's
+        // first two blocks share the HBM queue and block 0 arrives later
         bool ok = mbar_wait_bounded(&bars[0], 0, kWaitCycles);
+        if (ok && wt == 0 && steps > 1) load_block(1);
         if (ok) h_block(0);
         failed = __syncthreads_or(!ok);  // H(0) is in hb[0]
         for (int t = 0; t < steps && !failed; ++t) {
