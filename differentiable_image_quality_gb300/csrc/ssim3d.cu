@@ -58,8 +58,9 @@ struct Geo {
 using GS = Geo<kXy3dX>;   // xy kernel
 using GA = Geo<kAdj3dX>;  // adjoint kernel
 
-constexpr int NBUF = 6;         // staged slices in flight
-constexpr int CBUF = NBUF + 1;  // adjoint: chain-rule pixel tiles in flight
+constexpr int NBUF = 6;            // xy kernel: staged slices in flight
+constexpr int NBUF_A = 3;          // adjoint kernel: staged derivative slices
+constexpr int CBUF_A = NBUF_A + 2; // adjoint kernel: chain-rule pixel tiles in flight
 constexpr unsigned kStatsTx = 2u * GS::IY * GS::IXP * sizeof(float);
 constexpr unsigned kAdjTx =
     unsigned(GA::IY * GA::GXP * sizeof(float4) + 2 * GA::CSTAGE * sizeof(float));
@@ -72,8 +73,8 @@ __device__ unsigned g_staging3d_status;  // bit 0: a staging wait ran out of tim
 constexpr size_t kStatsInBytes = size_t(2) * NBUF * GS::XSTAGE * sizeof(float);
 constexpr size_t kStatsXBytes = size_t(2) * GS::IY * GS::HXP * sizeof(float4);
 constexpr size_t kStatsYBytes = size_t(2) * GS::TY * GS::TX * sizeof(float4);  // two slices
-constexpr size_t kAdjInBytes = size_t(NBUF) * GA::GSTAGE * sizeof(float4);
-constexpr size_t kChainBytes = size_t(2) * CBUF * GA::CSTAGE * sizeof(float);
+constexpr size_t kAdjInBytes = size_t(NBUF_A) * GA::GSTAGE * sizeof(float4);
+constexpr size_t kChainBytes = size_t(2) * CBUF_A * GA::CSTAGE * sizeof(float);
 constexpr size_t kAdjXBytes = size_t(2) * GA::IY * GA::HXP * sizeof(float4);
 constexpr size_t kAdjYBytes = size_t(2) * GA::TY * GA::TX * sizeof(float4);
 
@@ -166,14 +167,16 @@ __device__ __forceinline__ float zshift1_zero(float (&P)[kTaps - 1])
     return out;
 }
 
-// Slices j < waited have been waited for, j < issued copied: after a failed
-// wait, let the copies still in flight land (bounded), then record the failure.
+// Slices j < waited have been waited for, j < issued copied (slice j on barrier
+// j % NB): after a failed wait, let the copies still in flight land (bounded),
+// then record the failure.
+template <int NB>
 __device__ __forceinline__ void drain_failed(uint64_t *bars, int waited, int issued)
 {
     const long long t0 = clock64();
     for (int j = waited; j < issued; ++j) {
         const long long left = kDrainCycles - (clock64() - t0);
-        if (left > 0) mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, left);
+        if (left > 0) mbar_wait_bounded(&bars[j % NB], (j / NB) & 1, left);
     }
     atomicOr(&g_staging3d_status, 1u);
 }
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
     }
     cp_async_wait<0>();
     if (failed) {
-        if (a.tma && tid == 0) drain_failed(bars, waited, issued);
+        if (a.tma && tid == 0) drain_failed<NBUF>(bars, waited, issued);
         if (col_ok)
             for (int s = 0; s < nz; ++s) tcol[s * tstride] = nan4();
     }
@@ -524,19 +527,19 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
 // ------------------------------------------------------------- adjoint kernel
 
 template <bool G2>
-__global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
+__global__ void __launch_bounds__(GA::NT, 3) ssim3d_adjoint_kernel(const __grid_constant__ Ssim3dArgs a)
 {
     constexpr int NT = GA::NT, TY = GA::TY, TX = GA::TX, IY = GA::IY, IX = GA::IX,
                   GXP = GA::GXP, HXP = GA::HXP, KX = GA::KX, NXI = GA::NXI, KY = GA::KY,
                   NYI = GA::NYI, GSTAGE = GA::GSTAGE, CSTAGE = GA::CSTAGE;
     extern __shared__ __align__(128) unsigned char smem_dyn[];
     unsigned char *smem_raw = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
-    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF][GSTAGE]
-    float *cbx = reinterpret_cast<float *>(smem_raw + kAdjInBytes);      // [CBUF][TY][TX]
-    float *cby = cbx + CBUF * CSTAGE;
+    float4 *gs = reinterpret_cast<float4 *>(smem_raw);                   // [NBUF_A][GSTAGE]
+    float *cbx = reinterpret_cast<float *>(smem_raw + kAdjInBytes);      // [CBUF_A][TY][TX]
+    float *cby = cbx + CBUF_A * CSTAGE;
     float4 *ux = reinterpret_cast<float4 *>(smem_raw + kAdjInBytes + kChainBytes);  // [2][IY][HXP]
     float4 *uy = ux + 2 * IY * HXP;                                       // [2][TY][TX]
-    __shared__ uint64_t bars[NBUF];
+    __shared__ uint64_t bars[NBUF_A];
     pdl_trigger();
     pdl_wait();  // ufield of the z kernel ahead on the stream
 
@@ -560,17 +563,17 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     const float scale = a.dL ? a.dL[n] * a.inv_count : a.inv_count;
 
     // derivative slice q0 + s and the input pixels of the same slice into
-    // chain buffer s % CBUF
+    // chain buffer s % CBUF_A
     auto load_slice = [&](int s) {
-        const int buf = s % NBUF;
+        const int buf = s % NBUF_A;
         const int q = q0 + s;
         if (a.tma_adj) {
             // zeros outside the derivative domain
             if (tid == 0) {
                 mbar_arrive_expect_tx(&bars[buf], kAdjTx + a.tx_extra);
                 tma_load_4d(gs + buf * GSTAGE, &a.tm_g, 4 * gx0, gy0, q, plane, &bars[buf]);
-                tma_load_4d(cbx + (s % CBUF) * CSTAGE, &a.tm_cx, x0, y0, q, plane, &bars[buf]);
-                tma_load_4d(cby + (s % CBUF) * CSTAGE, &a.tm_cy, x0, y0, q, plane, &bars[buf]);
+                tma_load_4d(cbx + (s % CBUF_A) * CSTAGE, &a.tm_cx, x0, y0, q, plane, &bars[buf]);
+                tma_load_4d(cby + (s % CBUF_A) * CSTAGE, &a.tm_cy, x0, y0, q, plane, &bars[buf]);
             }
             return;
         }
@@ -585,8 +588,8 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
         const int qy = y0 + ty, qx = x0 + tx;
         const bool inb = (qy < a.H) && (qx < a.W);
         const size_t gi = inb ? plane_off + (size_t(q) * a.H + qy) * a.W + qx : 0;
-        cp_async4(cbx + (s % CBUF) * CSTAGE + tid, a.x + gi, inb);
-        cp_async4(cby + (s % CBUF) * CSTAGE + tid, a.y + gi, inb);
+        cp_async4(cbx + (s % CBUF_A) * CSTAGE + tid, a.x + gi, inb);
+        cp_async4(cby + (s % CBUF_A) * CSTAGE + tid, a.y + gi, inb);
     };
 
     // adjoint row pass: gradient columns [KX g, KX g + KX) of staged row r
@@ -595,7 +598,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     auto x_item = [&](int s, int item) {
         const int g = item / IY, r = item - g * IY;
         float2 oa[KX], ob[KX];
-        const float4 *src = gs + (s % NBUF) * GSTAGE + r * GXP + g * KX;
+        const float4 *src = gs + (s % NBUF_A) * GSTAGE + r * GXP + g * KX;
         if (G2) {
             taps4<KX>(src, 1, oa, ob);
         } else {
@@ -637,29 +640,33 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
         if (!col_ok) return;
         const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
         const size_t gi = gbase + size_t(q0 + s) * gstride;
-        const float x = cbx[(s % CBUF) * CSTAGE + tid] - kShift;
-        const float y = cby[(s % CBUF) * CSTAGE + tid] - kShift;
+        const float x = cbx[(s % CBUF_A) * CSTAGE + tid] - kShift;
+        const float y = cby[(s % CBUF_A) * CSTAGE + tid] - kShift;
         a.out1[gi] = scale * fmaf(2.0f * x, h.y, fmaf(y, h.z, h.x));
         if (G2) a.out2[gi] = scale * fmaf(2.0f * y, h.y, fmaf(x, h.z, h.w));
     };
 
-    // The pipeline of the xy kernel, with the chain rule in place of the
-    // store.  Chain buffer (s + NBUF) % CBUF, filled at step s, held slice
-    // s - 1's pixels, read by the chain rule of the step before.
+    // The pipeline of the xy kernel, with the chain rule in place of the store,
+    // on NBUF_A staging buffers: at step s the chain rule of slice s, the column
+    // pass of slice s + 1 and the row pass of slice s + 2 run; the buffer whose
+    // row pass ran in the step before (slice s + 1) takes slice s + 1 + NBUF_A as
+    // the step starts, two steps before its row pass.  Chain tiles live from the
+    // slice's copy to its chain rule: NBUF_A + 2 of them.  With cp.async staging
+    // every wait leaves the one newest group pending.
     auto landed = [&](int j) {
-        return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
+        return j >= nz || mbar_wait_bounded(&bars[j % NBUF_A], (j / NBUF_A) & 1, kWaitCycles);
     };
     if (a.tma_adj) {
         if (tid == 0) {
 #pragma unroll
-            for (int b2 = 0; b2 < NBUF; ++b2) mbar_init(&bars[b2], 1);
+            for (int b2 = 0; b2 < NBUF_A; ++b2) mbar_init(&bars[b2], 1);
             mbar_init_fence();
         }
         __syncthreads();
     }
     int issued = 0, waited = 0;
 #pragma unroll
-    for (int k = 0; k < NBUF; ++k) {
+    for (int k = 0; k < NBUF_A; ++k) {
         if (k < nz) {
             load_slice(k);
             ++issued;
@@ -668,24 +675,35 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     }
     bool ok = true;
     if (a.tma_adj) ok = landed(0) && landed(1);
-    else cp_async_wait<NBUF - 2>();  // slices 0 and 1
+    else cp_async_wait<1>();  // slices 0 and 1
     bool failed = __syncthreads_or(!ok);
     if (!failed) {
         waited = min(nz, 2);
         for (int i = tid; i < NXI; i += NT) x_item(0, i);
         __syncthreads();
+        // slice 0's buffer is free: slice NBUF_A
+        if (NBUF_A < nz) {
+            load_slice(NBUF_A);
+            ++issued;
+        }
+        cp_async_commit();
         const int nx = (1 < nz) ? NXI : 0;
         for (int i = tid; i < NYI + nx; i += NT) {
             if (i < NYI) y_item(0, i);
             else x_item(1, i - NYI);
         }
         if (a.tma_adj) ok = landed(2);
-        else cp_async_wait<NBUF - 3>();  // slice 2
+        else cp_async_wait<1>();  // slice 2
         failed = __syncthreads_or(!ok);
         if (!failed) waited = min(nz, 3);
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
+        if (s + 1 + NBUF_A < nz) {
+            load_slice(s + 1 + NBUF_A);
+            ++issued;
+        }
+        cp_async_commit();
         chain_step(s);
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
@@ -693,13 +711,8 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
             if (i < ny) y_item(s + 1, i);
             else x_item(s + 2, i - ny);
         }
-        if (s + NBUF < nz) {
-            load_slice(s + NBUF);
-            ++issued;
-        }
-        cp_async_commit();
         if (a.tma_adj) ok = landed(s + 3);
-        else cp_async_wait<NBUF - 3>();  // slice s + 3 (and its chain tile) landed
+        else cp_async_wait<1>();  // slice s + 3 (and its chain tile) landed
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
@@ -708,7 +721,7 @@ __global__ void __launch_bounds__(GA::NT, 2) ssim3d_adjoint_kernel(const __grid_
     }
     cp_async_wait<0>();
     if (failed) {
-        if (a.tma_adj && tid == 0) drain_failed(bars, waited, issued);
+        if (a.tma_adj && tid == 0) drain_failed<NBUF_A>(bars, waited, issued);
         if (col_ok)
             for (int s = 0; s < nz; ++s) {
                 const size_t gi = gbase + size_t(q0 + s) * gstride;
