@@ -58,7 +58,7 @@ struct Geo {
 using GS = Geo<kXy3dX>;   // xy kernel
 using GA = Geo<kAdj3dX>;  // adjoint kernel
 
-constexpr int NBUF = 6;            // xy kernel: staged slices in flight
+constexpr int NBUF = 3;            // xy kernel: staged slices
 constexpr int NBUF_A = 3;          // adjoint kernel: staged derivative slices
 constexpr int CBUF_A = NBUF_A + 2; // adjoint kernel: chain-rule pixel tiles in flight
 constexpr unsigned kStatsTx = 2u * GS::IY * GS::IXP * sizeof(float);
@@ -316,10 +316,13 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
     // the row pass of slice s + 2, then one barrier.  The row and column results
     // are double-buffered by slice parity, so each buffer a step writes was last
     // read in the step before.  Slices 0 .. NBUF-1 are in flight from the start
-    // (one commit group each); slice s + NBUF is issued at step s into the
-    // buffer the row pass of slice s released two steps earlier.  Tensor
-    // staging waits on slice j's barrier (use j / NBUF of buffer j % NBUF); a
-    // wait that runs out stops the walk and the block's slices come out NaN.
+    // (one commit group each) and slice NBUF follows the row pass of slice 0;
+    // as step s starts, the buffer whose row pass ran in the step before (slice
+    // s + 1) takes slice s + 1 + NBUF, NBUF - 1 steps ahead of its row pass.
+    // With cp.async staging every wait leaves the one newest group pending.
+    // Tensor staging waits on slice j's barrier (use j / NBUF of buffer
+    // j % NBUF); a wait that runs out stops the walk and the block's slices
+    // come out NaN.
     auto landed = [&](int j) {
         return j >= nz || mbar_wait_bounded(&bars[j % NBUF], (j / NBUF) & 1, kWaitCycles);
     };
@@ -348,18 +351,28 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
         waited = min(nz, 2);
         for (int i = tid; i < NXI; i += NT) x_item(0, i);
         __syncthreads();
+        if (NBUF < nz) {  // slice 0's buffer is free
+            load_slice(NBUF);
+            ++issued;
+        }
+        cp_async_commit();
         const int nx = (1 < nz) ? NXI : 0;
         for (int i = tid; i < NYI + nx; i += NT) {
             if (i < NYI) y_item(0, i);
             else x_item(1, i - NYI);
         }
         if (a.tma) ok = landed(2);
-        else cp_async_wait<NBUF - 3>();  // slice 2
+        else cp_async_wait<NBUF - 2>();  // slice 2
         failed = __syncthreads_or(!ok);
         if (!failed) waited = min(nz, 3);
     }
 
     for (int s = 0; s < nz && !failed; ++s) {
+        if (s + 1 + NBUF < nz) {
+            load_slice(s + 1 + NBUF);
+            ++issued;
+        }
+        cp_async_commit();
         if (col_ok) tcol[s * tstride] = hy[((s & 1) * TY + ty) * TX + tx];
         const int ny = (s + 1 < nz) ? NYI : 0;
         const int nx = (s + 2 < nz) ? NXI : 0;
@@ -367,13 +380,8 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
             if (i < ny) y_item(s + 1, i);
             else x_item(s + 2, i - ny);
         }
-        if (s + NBUF < nz) {
-            load_slice(s + NBUF);
-            ++issued;
-        }
-        cp_async_commit();
         if (a.tma) ok = landed(s + 3);
-        else cp_async_wait<NBUF - 3>();  // slice s + 3 has landed
+        else cp_async_wait<NBUF - 2>();  // slice s + 3 has landed
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
