@@ -284,25 +284,33 @@ def whole_job_rate(units_per_rank: float, world: int, steps: int, max_ms: float)
     return world * units_per_rank * steps / (max_ms / 1e3)
 
 
-def kernel_source_digest():
+# The sources that build the kernels a profile summary covers: its traffic
+# figure stands while these are unchanged.
+PROFILE_SOURCES = {
+    PROFILE: ("common.cuh", "ssim2d.cuh", "ssim2d.cu"),
+    PROFILE3D: ("common.cuh", "ssim2d.cuh", "ssim3d.cuh", "ssim3d.cu"),
+}
+
+
+def kernel_source_digest(names):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "differentiable_image_quality_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(path=PROFILE):
     """DRAM bytes per launch of the profiled kernel(s) from a committed ncu
-    summary, if it was taken from the current kernel sources; else None."""
+    summary, if it was taken from the current sources of those kernels; else
+    None."""
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_digest():
+    if not m or not s or s.group(1) != kernel_source_digest(PROFILE_SOURCES[path]):
         return None
     return float(m.group(1))
 
