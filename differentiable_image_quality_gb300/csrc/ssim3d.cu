@@ -32,10 +32,12 @@
 namespace gbssim {
 namespace {
 
-// Tile geometry of a slice kernel: TY x TX columns, one thread per column.  The
-// xy kernel runs 16 x 8 tiles (128 threads), the adjoint kernel 16 x 16 tiles
-// (256 threads).
-template <int TX_, int KY_>
+// Tile geometry of a slice kernel: TY x TX columns, one thread per column; a
+// row-pass item covers KX columns of one row, a column-pass item KY rows of
+// one column (wider items load fewer shared values per output).  The xy kernel
+// runs 16 x 8 tiles (128 threads) with 4 x 4 items, the adjoint kernel 16 x 16
+// tiles (256 threads) with row items of 8 columns and column items of 4 rows.
+template <int TX_, int KY_, int KX_>
 struct Geo {
     static constexpr int TY = kTile3dY, TX = TX_, NT = TY * TX;
     static constexpr int IY = TY + 10, IX = TX + 10;  // staged slice tile
@@ -44,7 +46,7 @@ struct Geo {
     static constexpr int IXU = (IX + 3) / 4, IXP = 4 * (IXU % 2 ? IXU : IXU + 1);
     static constexpr int GXP = IX + 1;  // float4 pitch of a staged derivative row (odd)
     static constexpr int HXP = TX + 1;  // float4 pitch of a row-pass output row
-    static constexpr int KX = 4, NXG = TX / KX, NXI = IY * NXG;  // row-pass items per slice
+    static constexpr int KX = KX_, NXG = TX / KX, NXI = IY * NXG;  // row-pass items per slice
     static constexpr int KY = KY_, NYG = TY / KY, NYI = NYG * TX;  // column-pass items per slice
     // staging buffers, each a multiple of 128 bytes (tensor-copy destinations)
     static constexpr int XSTAGE = (IY * IXP + 31) / 32 * 32;  // floats of a staged input tile
@@ -55,8 +57,8 @@ struct Geo {
     static_assert(IXP % 4 == 0 && IXP >= IX, "input pitch");
     static_assert((CSTAGE * 4) % 128 == 0, "chain tiles stay 128-byte aligned");
 };
-using GS = Geo<kXy3dX, 4>;   // xy kernel
-using GA = Geo<kAdj3dX, 4>;  // adjoint kernel
+using GS = Geo<kXy3dX, 4, 4>;   // xy kernel
+using GA = Geo<kAdj3dX, 4, 8>;  // adjoint kernel
 
 constexpr int NBUF = 3;            // xy kernel: staged slices
 constexpr int NBUF_A = 3;          // adjoint kernel: staged derivative slices
