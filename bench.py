@@ -293,11 +293,15 @@ PROFILE_SOURCES = {
 
 
 def kernel_source_digest(names):
+    """Digest of the named sources with their comments and blank lines taken
+    out (a comment cannot change a kernel's traffic)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "differentiable_image_quality_gb300", "csrc")
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        code = [ln.split("//", 1)[0].rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,7 +9,8 @@
 //        float4 per (slice, output column); the slice tiles are staged by
 //        tensor copies (one thread issues them, a transaction barrier per
 //        buffer tracks them, every wait bounded) or by cp.async where the tile
-//        does not start on a 16-byte column, NBUF slices in flight;
+//        does not start on a 16-byte column, into three buffers, each refilled
+//        two steps before its row pass;
 //   z    one thread per output column walks along Z: the Z window sums as a
 //        shift register of pending sums, SSIM (mean, map) and, for gradients,
 //        the derivatives of SSIM with respect to the four shifted moments,
