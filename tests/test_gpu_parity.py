@@ -151,6 +151,34 @@ def test_parity_forced_row_segments(dev, oracle_mod, padding, seg_rows):
             lib.gbssim_tune_seg_rows(0)
 
 
+@pytest.mark.parametrize("padding", ["valid", "same"])
+def test_pixels_do_not_depend_on_the_plan(dev, padding):
+    """The 2D kernels' bands lie on one 11-row grid per image, so every window's
+    shift, and with it every map value and gradient element, comes out the same
+    bit for bit whatever the row segmentation (forced here to several lengths,
+    some not multiples of 11).  The means sum per-segment partials, grouped by
+    the plan: they may differ in their last bits."""
+    from differentiable_image_quality_gb300 import _abi
+
+    x, y = uniform_pair((1, 2, 150, 300), 700, std=0.1)
+    dl = np.array([-1.0])
+    runs = []
+    with _abi.using_test_library() as lib:
+        for seg_rows in (0, 22, 30, 47):
+            lib.gbssim_tune_seg_rows(seg_rows)
+            try:
+                runs.append([_run(dev, x, y, dl, padding, True, path, want_map=True)
+                             for path in ("saved", "recompute")])
+            finally:
+                lib.gbssim_tune_seg_rows(0)
+    for seg_rows, got in zip((22, 30, 47), runs[1:]):
+        for g, r, path in zip(got, runs[0], ("saved", "recompute")):
+            label = f"{padding} seg_rows={seg_rows} {path}"
+            assert np.array_equal(g["map"], r["map"]), label
+            assert np.array_equal(g["g1"], r["g1"]) and np.array_equal(g["g2"], r["g2"]), label
+            assert np.max(np.abs(g["mean"] - r["mean"])) <= 1e-6, label
+
+
 @pytest.mark.parametrize("shape,padding,seed", [
     ((1, 3, 64, 64), "valid", 31), ((2, 2, 37, 300), "same", 32), ((1, 1, 250, 256), "valid", 33),
     ((1, 2, 130, 236), "same", 34), ((1, 1, 11, 12), "valid", 35)])
