@@ -169,29 +169,35 @@ __device__ __forceinline__ float rcp_approx(float x)
 // ------------------------------------------------------------ SSIM at a pixel
 
 // Statistics of one window in shifted form: m1 = E[x'], m2 = E[y'],
-// es = E[x'^2] + E[y'^2], e12 = E[x'y'], with x' = x - s, y' = y - t for the
-// window's shift sh = (s, t).
+// es = E[x'^2] + E[y'^2], ed = E[(x' - y')^2], with x' = x - s, y' = y - t for
+// the window's shift sh = (s, t).  The fourth statistic is the blurred squared
+// difference rather than E[x'y'] (which is (es - ed) / 2): SSIM's
+// contrast-structure term is
+//   cs = (2 sigma12 + C2) / (sigma_sum + C2) = 1 - D / (sigma_sum + C2),
+//   D = sigma_sum - 2 sigma12 = ed - (m1 - m2)^2,
+// and D, taken from ed, carries no rounding of the images' common level: where
+// the two images agree it is near zero whatever the shift, while es - 2 E[x'y']
+// would cancel two terms of the size of the shifted values squared.
 struct Moments {
-    float m1, m2, es, e12;
+    float m1, m2, es, ed;
 };
 
-// Upstream gradients of S with respect to the shifted moments (m1, m2, es, e12).
+// Upstream gradients of S with respect to the shifted moments (m1, m2, es, ed).
 // Because sigma11 and sigma22 enter S only as their sum, dS/dE[x'^2] and
-// dS/dE[y'^2] are one value, g_e.
+// dS/dE[y'^2] are one value, g_es.  In a flat window g_ed is of order 1 / C2
+// and g_es small; the chain rule meets g_ed only through x - y (see the
+// backward passes).
 struct MomentGrads {
-    float g_m1, g_m2, g_e, g_e12;
+    float g_m1, g_m2, g_es, g_ed;
 };
 
-// S = A1 A2 / (B1 B2) with
-//   mu = m + sh, sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2,
-//   A1 = 2 mu1 mu2 + C1, A2 = 2 sigma12 + C2, B1 = mu1^2 + mu2^2 + C1,
-//   B2 = sigma_sum + C2.
-// The four factors A1, A2, B1, B2 of S from the shifted moments, each product
-// fused into the sum that uses it (one rounding per term):
-//   B1 = mu1^2 + mu2^2 + C1, B2 = (es + C2) - m1^2 - m2^2,
-//   A1 = 2 mu1 mu2 + C1,     A2 = 2 (e12 - m1 m2) + C2.
+// S = l * cs with
+//   mu = m + sh, sigma_sum = es - m1^2 - m2^2, D = ed - (m1 - m2)^2,
+//   l = A1 / B1, A1 = 2 mu1 mu2 + C1, B1 = mu1^2 + mu2^2 + C1,
+//   cs = 1 - D / B2, B2 = sigma_sum + C2,
+// each product fused into the sum that uses it (one rounding per term).
 struct SsimTerms {
-    float mu1, mu2, A1, A2, B1, B2;
+    float mu1, mu2, A1, B1, B2, D;
 };
 
 __device__ __forceinline__ SsimTerms ssim_terms(const Moments &m, float2 sh)
@@ -202,46 +208,49 @@ __device__ __forceinline__ SsimTerms ssim_terms(const Moments &m, float2 sh)
     t.B1 = fmaf(t.mu1, t.mu1, fmaf(t.mu2, t.mu2, kC1));
     t.B2 = fmaf(-m.m1, m.m1, fmaf(-m.m2, m.m2, m.es + kC2));
     t.A1 = fmaf(t.mu1 + t.mu1, t.mu2, kC1);
-    t.A2 = fmaf(2.0f, fmaf(-m.m1, m.m2, m.e12), kC2);
+    const float dm = m.m1 - m.m2;
+    t.D = fmaf(-dm, dm, m.ed);
     return t;
+}
+
+// The two factors of S: (l, cs).
+__device__ __forceinline__ float2 ssim_factors(const Moments &m, float2 sh)
+{
+    const SsimTerms t = ssim_terms(m, sh);
+    return make_float2(t.A1 * rcp_approx(t.B1), fmaf(-t.D, rcp_approx(t.B2), 1.0f));
 }
 
 __device__ __forceinline__ float ssim_value(const Moments &m, float2 sh)
 {
-    const SsimTerms t = ssim_terms(m, sh);
-    return (t.A1 * t.A2) * rcp_approx(t.B1 * t.B2);
+    const float2 lc = ssim_factors(m, sh);
+    return lc.x * lc.y;
 }
 
-// The two factors of S: (l, cs) = (A1 / B1, A2 / B2), S = l * cs.
-__device__ __forceinline__ float2 ssim_factors(const Moments &m, float2 sh)
-{
-    const SsimTerms t = ssim_terms(m, sh);
-    return make_float2(t.A1 * rcp_approx(t.B1), t.A2 * rcp_approx(t.B2));
-}
-
-// S and its derivatives with respect to the shifted moments, written as
-// S = l * cs with l = A1 / B1 (luminance) and cs = A2 / B2 (contrast-structure):
-//   dS/dsigma_sum = -cs * l / B2,   dS/dsigma12 = 2 l / B2,
-//   dS/dmu1 (sigmas fixed) = 2 cs (mu2 - mu1 l) / B1,
-// and through sigma_sum = es - m1^2 - m2^2, sigma12 = e12 - m1 m2:
-//   dS/dm1 = dS/dmu1 - 2 m1 dS/dsigma_sum - m2 dS/dsigma12
-//          = 2 cs (mu2 - mu1 l) / B1 + (2 l / B2) (m1 cs - m2)        (m2 likewise).
+// S and its derivatives with respect to the shifted moments:
+//   dS/des = l D / B2^2,   dS/ded = -l / B2,
+//   dS/dmu1 (sigma_sum and D fixed) = 2 cs (mu2 - mu1 l) / B1,
+// and through sigma_sum = es - m1^2 - m2^2, D = ed - (m1 - m2)^2:
+//   dS/dm1 = 2 cs (mu2 - mu1 l) / B1 - 2 m1 dS/des - 2 (m1 - m2) dS/ded,
+//   dS/dm2 = 2 cs (mu1 - mu2 l) / B1 - 2 m2 dS/des + 2 (m1 - m2) dS/ded.
 // When `valid` is false every derivative (and S) comes out as exactly zero:
-// l and cs are zeroed before they are used.
+// l is zeroed before it is used.
 template <bool WANT_G2>
 __device__ __forceinline__ float ssim_and_grads(const Moments &m, float2 sh, bool valid,
                                                 MomentGrads &g)
 {
     const SsimTerms t = ssim_terms(m, sh);
     const float r1 = rcp_approx(t.B1), r2 = rcp_approx(t.B2);
-    const float l = valid ? t.A1 * r1 : 0.0f, cs = valid ? t.A2 * r2 : 0.0f;
+    const float l = valid ? t.A1 * r1 : 0.0f;
+    const float Dr2 = t.D * r2;
+    const float cs = 1.0f - Dr2;
     const float S = l * cs;
     const float lr2 = l * r2;
-    g.g_e = -cs * lr2;
-    g.g_e12 = lr2 + lr2;
-    const float cr1x2 = cs * (r1 + r1);
-    g.g_m1 = fmaf(cr1x2, fmaf(-t.mu1, l, t.mu2), g.g_e12 * fmaf(m.m1, cs, -m.m2));
-    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-t.mu2, l, t.mu1), g.g_e12 * fmaf(m.m2, cs, -m.m1));
+    g.g_ed = -lr2;
+    g.g_es = lr2 * Dr2;
+    const float cr1x2 = valid ? cs * (r1 + r1) : 0.0f;
+    const float dm2 = (m.m1 - m.m2) * 2.0f;
+    g.g_m1 = fmaf(cr1x2, fmaf(-t.mu1, l, t.mu2), fmaf(-2.0f * m.m1, g.g_es, -dm2 * g.g_ed));
+    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-t.mu2, l, t.mu1), fmaf(-2.0f * m.m2, g.g_es, dm2 * g.g_ed));
     return S;
 }
 

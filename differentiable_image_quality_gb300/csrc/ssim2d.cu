@@ -7,7 +7,10 @@
 //             column pass, SSIM in registers, and the mean;
 //   backward  the blur's adjoint (a "full" correlation) applied to the upstream
 //             gradients of the statistics, then the chain rule
-//             grad1 = B^T g_mu1 + 2 x B^T g_e + y B^T g_e12 (grad2 likewise).
+//             grad1 = B^T g_mu1 + 2 x B^T g_e + y B^T g_e12 (grad2 likewise),
+//             evaluated here with the derivatives of S with respect to
+//             es = E[x^2] + E[y^2] and ed = E[(x - y)^2] (E[xy] = (es - ed) / 2):
+//             grad1 = B^T g~_m1 + 2 (x - 1/2) B^T g_es + 2 (x - y) B^T g_ed.
 //
 // Design.  A CTA owns a vertical strip of columns of one (n, c) plane and walks
 // down a segment of its rows, 11 rows per step.  Per step:
@@ -26,7 +29,7 @@
 //
 // The window sums run on pairs of float32 values with packed instructions
 // (fma.rn.f32x2 and friends): the statistics as (mu1, mu2) and (E[x^2]+E[y^2],
-// E[xy]), the adjoint maps as (g_mu1, g_e) and (g_e12, g_mu2).  The column
+// E[(x-y)^2]), the adjoint maps as (g_mu1, g_es) and (g_ed, g_mu2).  The column
 // passes use the window's symmetry (w_k = w_{10-k}): five paired sums, then six
 // multiply-adds, which also halves the length of each dependent chain.
 //
@@ -100,11 +103,11 @@ __device__ __forceinline__ int stat_shift(int off) { return (4 - (off & 3)) & 3;
 
 // Shared memory (byte offsets):
 //   xs, ys  [NBUF][XB] float               input rows: STEP rows of IWP floats
-//   hb      [HBUF] float4                  row-blurred statistics (m1, m2, es, e12)
+//   hb      [HBUF] float4                  row-blurred statistics (m1, m2, es, ed)
 // gradient mode only:
-//   va      [STEP][P2] float2              adjoint column sums (g_m1, g_e)
-//   vb2     [STEP][P2] float2              (g_e12, g_m2)        [grad2]
-//   vc      [STEP][P1] float               g_e12                [grad1 only]
+//   va      [STEP][P2] float2              adjoint column sums (g_m1, g_es)
+//   vb2     [STEP][P2] float2              (g_ed, g_m2)         [grad2]
+//   vc      [STEP][P1] float               g_ed                 [grad1 only]
 //   cbx,cby [CBB] float                    input pixels of this step's gradient rows,
 //                                          STEP rows of CBP floats
 // Every buffer starts on a 128-byte boundary (tensor-copy destinations).
@@ -398,14 +401,15 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             yv[KH + 8] = v.x; yv[KH + 9] = v.y;
         }
         const float2 sh = shift_of(below(t) ? t - 1 : t, g);
-        float2 accA[KH], accB[KH];  // (m1, m2), (es, e12)
+        float2 accA[KH], accB[KH];  // (m1, m2), (es, ed)
 #pragma unroll
         for (int m = 0; m < KH + 10; ++m) {
             // two scalar subtractions: x and y come from different loads, and a
             // packed subtraction would first have to move them into one pair
             const float2 p = f2(xv[m] - sh.x, yv[m] - sh.y);
             const float2 sq = __fmul2_rn(p, p);
-            const float2 q = f2(sq.x + sq.y, p.x * p.y);
+            const float dd = p.x - p.y;
+            const float2 q = f2(sq.x + sq.y, dd * dd);
 #pragma unroll
             for (int o = 0; o < KH; ++o) {
                 const int b = m - o;
@@ -435,9 +439,9 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         const int g = item / STEP, k = item - g * STEP;
         const int q = R0 + (a_step * STEP) + k - 10;
         if (q < q0 || q >= q1) return;
-        float2 accA[KA];             // (B^T g_m1, B^T g_e)
-        float2 accB[KA];             // (B^T g_e12, B^T g_m2)   [G2]
-        float accC[KA];              // B^T g_e12              [grad1 only]
+        float2 accA[KA];             // (B^T g_m1, B^T g_es)
+        float2 accB[KA];             // (B^T g_ed, B^T g_m2)    [G2]
+        float accC[KA];              // B^T g_ed               [grad1 only]
         const float2 *pa = va + k * P2 + g * KA;   // 16-byte aligned (g * KA even)
 #pragma unroll
         for (int m = 0; m < KA + 10; m += 2) {
@@ -489,9 +493,12 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             }
         }
         // chain rule with the prefetched pixels (cb columns jj + CBOFF: 8-byte
-        // aligned), in the form grad1 = B^T g~_m1 + 2 (x - 1/2) B^T g_e +
-        // (y - 1/2) B^T g_e12: each window's own shift is folded into g~_m1 (and
-        // g~_m2) by the column pass, so the pixels here all take 1/2
+        // aligned).  Per window p (shift (s, t)) and pixel r the term is
+        //   g_m1 + 2 (x - s) g_es + 2 ((x - s) - (y - t)) g_ed
+        //     = g~_m1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed,
+        // g~_m1 being formed by the column pass, so the pixels here need no
+        // shift.  In a flat window g_ed is of order 1 / C2 and meets x - y,
+        // small where the two images agree; g_es is small there.
         const float *px = cbx + k * CBP + CBOFF + g * KA;
         const float *py = cby + k * CBP + CBOFF + g * KA;
         float r1[KA], r2[KA];
@@ -499,14 +506,15 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         for (int o = 0; o < KA; o += 2) {
             const float2 xx = *reinterpret_cast<const float2 *>(px + o);
             const float2 yy = *reinterpret_cast<const float2 *>(py + o);
-            const float xo[2] = {xx.x - kShift, xx.y - kShift};
-            const float yo[2] = {yy.x - kShift, yy.y - kShift};
+            const float xv[2] = {xx.x, xx.y};
+            const float yv[2] = {yy.x, yy.y};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int oo = o + h;
-                const float e12 = G2 ? accB[oo].x : accC[oo];
-                r1[oo] = scale * fmaf(2.0f * xo[h], accA[oo].y, fmaf(yo[h], e12, accA[oo].x));
-                if (G2) r2[oo] = scale * fmaf(2.0f * yo[h], accA[oo].y, fmaf(xo[h], e12, accB[oo].y));
+                const float ged = G2 ? accB[oo].x : accC[oo];
+                const float dxy2 = 2.0f * (xv[h] - yv[h]);
+                r1[oo] = scale * fmaf(dxy2, ged, fmaf(2.0f * (xv[h] - kShift), accA[oo].y, accA[oo].x));
+                if (G2) r2[oo] = scale * fmaf(-dxy2, ged, fmaf(2.0f * (yv[h] - kShift), accA[oo].y, accB[oo].y));
             }
         }
         const size_t rowg = plane_off + size_t(q) * a.W;
@@ -533,10 +541,10 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         }
     };
     // ---- column pass state: registers of thread tid (statistic column sc0 + tid)
-    float2 hA[STEP], hB[STEP];   // row-blurred (m1, m2), (es, e12)
-    float2 gA[STEP];             // (g_m1, g_e)
-    float2 gB[STEP];             // (g_e12, g_m2)   [G2]
-    float gC[STEP];              // g_e12           [grad1 only]
+    float2 hA[STEP], hB[STEP];   // row-blurred (m1, m2), (es, ed)
+    float2 gA[STEP];             // (g_m1, g_es)
+    float2 gB[STEP];             // (g_ed, g_m2)    [G2]
+    float gC[STEP];              // g_ed            [grad1 only]
 #pragma unroll
     for (int k = 0; k < STEP; ++k) {
         hA[k] = hB[k] = gA[k] = gB[k] = f2(0.f, 0.f);
@@ -569,7 +577,7 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
     // move them to the new one (d = old - new): with x' = x - s_old,
     //   E[x' + dx] = m1 + dx,
     //   E[(x' + dx)^2] + E[(y' + dy)^2] = es + dx (2 m1 + dx) + dy (2 m2 + dy),
-    //   E[(x' + dx)(y' + dy)] = e12 + dx (m2 + dy) + dy m1,
+    //   E[(x' - y' + dd)^2] = ed + dd (2 (m1 - m2) + dd),   dd = dx - dy,
     // exact because every row-pass window's weights sum to one.  The two
     // corrections of es are summed before es is touched: where the old shift was
     // far from the rows' values they nearly cancel es, and one rounding of es
@@ -582,7 +590,8 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
             const float2 v = __fmul2_rn(__ffma2_rn(f2(2.f, 2.f), m, d), d);
             float2 e = hB[k];
             e.x = e.x + (v.x + v.y);
-            e.y = fmaf(d.y, m.x, fmaf(d.x, m.y + d.y, e.y));
+            const float dd = d.x - d.y;
+            e.y = fmaf(dd, fmaf(2.0f, m.x - m.y, dd), e.y);
             hB[k] = e;
             hA[k] = __fadd2_rn(m, d);
         }
@@ -640,16 +649,18 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         if (GRAD) {
             MomentGrads gg;
             const float S = ssim_and_grads<G2>(mo, sh, ok, gg);
-            // fold the window's shift into the first map (the chain rule uses
-            // x - 1/2, y - 1/2 for every pixel):
-            //   g~_m1 = g_m1 + 2 (1/2 - s) g_e + (1/2 - t) g_e12   (g~_m2 likewise)
-            const float g1 = fmaf(1.0f - 2.0f * sh.x, gg.g_e, fmaf(0.5f - sh.y, gg.g_e12, gg.g_m1));
-            gA[k] = f2(g1, gg.g_e);
+            // fold the window's shift into the first map (see the chain rule in
+            // the adjoint row pass):
+            //   g~_m1 = g_m1 + 2 (1/2 - s) g_es - 2 (s - t) g_ed
+            //   g~_m2 = g_m2 + 2 (1/2 - t) g_es + 2 (s - t) g_ed
+            const float dst2 = 2.0f * (sh.x - sh.y);
+            const float g1 = fmaf(1.0f - 2.0f * sh.x, gg.g_es, fmaf(-dst2, gg.g_ed, gg.g_m1));
+            gA[k] = f2(g1, gg.g_es);
             if (G2) {
-                const float g2 = fmaf(1.0f - 2.0f * sh.y, gg.g_e, fmaf(0.5f - sh.x, gg.g_e12, gg.g_m2));
-                gB[k] = f2(gg.g_e12, g2);
+                const float g2 = fmaf(1.0f - 2.0f * sh.y, gg.g_es, fmaf(dst2, gg.g_ed, gg.g_m2));
+                gB[k] = f2(gg.g_ed, g2);
             } else {
-                gC[k] = gg.g_e12;
+                gC[k] = gg.g_ed;
             }
             const bool own = ok && col_own && (k >= kown);
             if (want_mean) {
@@ -660,13 +671,16 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
                 // the window's statistics and the derivatives of S with respect
                 // to the unshifted moments mu1, mu2, E[x^2] (= E[y^2]), E[xy]
                 const size_t o = (size_t(plane) * a.Ho + p) * a.Wo + pc;
+                // (es and ed each hold E[x^2] + E[y^2] once; ed holds -2 E[xy])
                 const float ss = mo.es - (mo.m1 * mo.m1 + mo.m2 * mo.m2);
-                const float s12 = fmaf(-mo.m1, mo.m2, mo.e12);
+                const float s12 = fmaf(-mo.m1, mo.m2, 0.5f * (mo.es - mo.ed));
                 reinterpret_cast<float4 *>(a.dump_stats)[o] =
                     make_float4(mo.m1 + sh.x, mo.m2 + sh.y, ss, s12);
-                const float dmu1 = fmaf(-2.0f * sh.x, gg.g_e, fmaf(-sh.y, gg.g_e12, gg.g_m1));
-                const float dmu2 = fmaf(-2.0f * sh.y, gg.g_e, fmaf(-sh.x, gg.g_e12, gg.g_m2));
-                reinterpret_cast<float4 *>(a.dump_grads)[o] = make_float4(dmu1, dmu2, gg.g_e, gg.g_e12);
+                const float dst2 = 2.0f * (sh.x - sh.y);
+                const float dmu1 = fmaf(-2.0f * sh.x, gg.g_es, fmaf(-dst2, gg.g_ed, gg.g_m1));
+                const float dmu2 = fmaf(-2.0f * sh.y, gg.g_es, fmaf(dst2, gg.g_ed, gg.g_m2));
+                reinterpret_cast<float4 *>(a.dump_grads)[o] =
+                    make_float4(dmu1, dmu2, gg.g_es + gg.g_ed, -2.0f * gg.g_ed);
             }
             va[k * P2 + tid] = ring_sum2<k>(gA);
             if (G2) vb2[k * P2 + tid] = ring_sum2<k>(gB);
@@ -909,7 +923,8 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
                         const float2 v = __fmul2_rn(__ffma2_rn(f2(2.f, 2.f), m, d), d);
                         float2 e = hB[k];
                         e.x = e.x + (v.x + v.y);
-                        e.y = fmaf(d.y, m.x, fmaf(d.x, m.y + d.y, e.y));
+                        const float dd = d.x - d.y;
+                        e.y = fmaf(dd, fmaf(2.0f, m.x - m.y, dd), e.y);
                         hB[k] = e;
                         hA[k] = __fadd2_rn(m, d);
                     }
@@ -980,7 +995,8 @@ __device__ __forceinline__ void fsplit_body(const Ssim2dArgs &a, int block)
             for (int m = 0; m < KW + 10; ++m) {
                 const float2 p = f2(xv[m] - sh.x, yv[m] - sh.y);
                 const float2 sq = __fmul2_rn(p, p);
-                const float2 q = f2(sq.x + sq.y, p.x * p.y);
+                const float dd = p.x - p.y;
+                const float2 q = f2(sq.x + sq.y, dd * dd);
 #pragma unroll
                 for (int o = 0; o < KW; ++o) {
                     const int b = m - o;

@@ -18,12 +18,14 @@
 //        window being symmetric) runs as a second shift register -> ufield;
 //   adj  per slice, the XY adjoint of those four fields on a tile plus halo
 //        in shared memory, then the chain rule
-//        grad1 = B^T g_mu1 + 2 x' B^T g_e + y' B^T g_e12 (grad2 likewise).
+//        grad1 = B^T g_mu1 + 2 x' B^T g_e + y' B^T g_e12 (grad2 likewise), taken
+//        with the derivatives with respect to es = E[x'^2] + E[y'^2] and
+//        ed = E[(x - y)^2]: B^T g_mu1 + 2 x' B^T g_es + 2 (x - y) B^T g_ed.
 // The page's own plan keeps the 2D convolution per slice and runs Z per depth
 // row in one kernel; walking Z inside the slice kernels re-runs the XY work of
 // each Z segment's 10-slice warm-up, which these passes avoid.
-// All window sums run on float pairs (fma.rn.f32x2): (mu1, mu2), (es, e12) for
-// the statistics, (g_mu1, g_e), (g_e12, g_mu2) for the adjoint.  Work items of
+// All window sums run on float pairs (fma.rn.f32x2): (mu1, mu2), (es, ed) for
+// the statistics, (g_mu1, g_es), (g_ed, g_mu2) for the adjoint.  Work items of
 // the row passes are numbered row-fastest over odd shared-memory pitches, so
 // the threads of a quarter warp hit distinct bank groups.
 #include "common.cuh"
@@ -109,7 +111,7 @@ __device__ __forceinline__ void taps4(const float4 *src, int stride, float2 (&oa
 }
 
 // The same pass over the first three components only (x, y as a pair, z
-// alone): the adjoint for grad_img1 needs B^T of g_mu1, g_e and g_e12, not g_mu2.
+// alone): the adjoint for grad_img1 needs B^T of g_mu1, g_es and g_ed, not g_mu2.
 template <int K>
 __device__ __forceinline__ void taps3(const float4 *src, int stride, float2 (&oa)[K], float (&oc)[K])
 {
@@ -282,7 +284,8 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
         for (int m = 0; m < KX + 10; ++m) {
             const float2 p = f2(xv[m] - kShift, yv[m] - kShift);
             const float2 sq = __fmul2_rn(p, p);
-            const float2 q = f2(sq.x + sq.y, p.x * p.y);
+            const float dd = p.x - p.y;
+            const float2 q = f2(sq.x + sq.y, dd * dd);
 #pragma unroll
             for (int o = 0; o < KX; ++o) {
                 const int t = m - o;
@@ -402,14 +405,15 @@ __global__ void __launch_bounds__(GS::NT, 4) ssim3d_xy_kernel(const __grid_const
 // ------------------------------------------------------------------- z kernel
 
 // Shifted statistics of a slice of padding (same padding, outside the volume):
-// every pixel is 0, i.e. -kShift after the shift, blurred by the XY window.
+// every pixel is 0, i.e. -kShift after the shift, blurred by the XY window (the
+// two images' difference is 0 there).
 __device__ __forceinline__ float4 pad_stats()
 {
     float t = 0.f;
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) t += tap(k);
     const float s2 = t * t;
-    return make_float4(-kShift * s2, -kShift * s2, 2.0f * kShift * kShift * s2, kShift * kShift * s2);
+    return make_float4(-kShift * s2, -kShift * s2, 2.0f * kShift * kShift * s2, 0.0f);
 }
 
 // One thread per output column (Ho x Wo, flattened) and z segment.  With
@@ -446,9 +450,9 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
     const size_t ostride = size_t(cols);
     float *mapc = a.map ? a.map + (size_t(plane) * a.Do) * cols + (col_ok ? c : 0) : nullptr;
 
-    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, e12)
-    float2 QA[kTaps - 1], QB[kTaps - 1];  // adjoint: of (g_m1, g_e), (g_e12, g_m2)
-    float QC[kTaps - 1];                  // adjoint: of g_e12 alone without grad_img2
+    float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, ed)
+    float2 QA[kTaps - 1], QB[kTaps - 1];  // adjoint: of (g_m1, g_es), (g_ed, g_m2)
+    float QC[kTaps - 1];                  // adjoint: of g_ed alone without grad_img2
 #pragma unroll
     for (int k = 0; k < kTaps - 1; ++k) {
         PA[k] = PB[k] = QA[k] = QB[k] = f2(0.f, 0.f);
@@ -475,11 +479,11 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
         if (GRAD) {
             MomentGrads g;
             S = ssim_and_grads<G2>(mo, make_float2(kShift, kShift), true, g);
-            const float2 vA = zshift2(QA, f2(g.g_m1, g.g_e));
+            const float2 vA = zshift2(QA, f2(g.g_m1, g.g_es));
             float2 vB = f2(0.f, 0.f);
             float v12 = 0.f;
-            if (G2) vB = zshift2(QB, f2(g.g_e12, g.g_m2));
-            else v12 = zshift1(QC, g.g_e12);
+            if (G2) vB = zshift2(QB, f2(g.g_ed, g.g_m2));
+            else v12 = zshift1(QC, g.g_ed);
             emit(p, vA, vB, v12);
         } else {
             S = ssim_value(mo, make_float2(kShift, kShift));
@@ -646,15 +650,19 @@ __global__ void __launch_bounds__(GA::NT, 3) ssim3d_adjoint_kernel(const __grid_
     const size_t gbase = plane_off + size_t(col_ok ? qy : 0) * a.W + qx;
     const size_t gstride = size_t(a.H) * a.W;
 
-    // chain rule of slice s: (B^T g_m1, B^T g_e, B^T g_e12, B^T g_m2) at this pixel
+    // chain rule of slice s from (B^T g_m1, B^T g_es, B^T g_ed, B^T g_m2) at this
+    // pixel: per window (shift 1/2 for both images),
+    //   g_m1 + 2 x' g_es + 2 (x' - y') g_ed = g_m1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed;
+    // in a flat window g_ed is of order 1 / C2 and meets x - y
     auto chain_step = [&](int s) {
         if (!col_ok) return;
         const float4 h = uy[((s & 1) * TY + ty) * TX + tx];
         const size_t gi = gbase + size_t(q0 + s) * gstride;
-        const float x = cbx[(s % CBUF_A) * CSTAGE + tid] - kShift;
-        const float y = cby[(s % CBUF_A) * CSTAGE + tid] - kShift;
-        a.out1[gi] = scale * fmaf(2.0f * x, h.y, fmaf(y, h.z, h.x));
-        if (G2) a.out2[gi] = scale * fmaf(2.0f * y, h.y, fmaf(x, h.z, h.w));
+        const float x = cbx[(s % CBUF_A) * CSTAGE + tid];
+        const float y = cby[(s % CBUF_A) * CSTAGE + tid];
+        const float dxy2 = 2.0f * (x - y);
+        a.out1[gi] = scale * fmaf(dxy2, h.z, fmaf(2.0f * (x - kShift), h.y, h.x));
+        if (G2) a.out2[gi] = scale * fmaf(-dxy2, h.z, fmaf(2.0f * (y - kShift), h.y, h.w));
     };
 
     // The pipeline of the xy kernel, with the chain rule in place of the store,

@@ -20,7 +20,7 @@ from workloads import dl_vector, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-MAP_TOL_3D = 2e-4
+MAP_TOL_3D = 3e-5
 GRAD_RTOL = 1e-4
 N_SAMPLES = 3000
 

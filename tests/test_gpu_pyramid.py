@@ -2,18 +2,15 @@
 
 Every call goes through the C ABI.  Bars: the per-image means of l, cs and S
 within 1e-5 of the oracle's (the loss's mean bar); the maps of octave 0 within
-2e-5 absolute (the 2D SSIM map's bar), those of the downscaled octaves within
-2e-4.  The kernels shift each window's values by one value per 11-row band and
-8-column group, exact in real arithmetic; float32 rounding then acts on the
-shifted second moments, up to 2 in size, and S divides that error by
-sigma11 + sigma22 + C2 >= 9e-4.  A flat window whose band value lies across an
-edge from most of its pixels (in the window's low-weight corner) sees the
-largest shifted moments; in the downscaled octaves features are smaller, so
-such windows are more frequent: measured 4.6e-5 .. 1.04e-4 at octaves 1..4 of
-the 1080p blob render (same padding: 1.04e-4 at octave 3), 1.4e-5 at octave 0.
-Bands lie on one 11-row grid per image, so the values do not depend on the
-launch plan.  The GPU downscales in float32, the oracle in double from the same
-float32 inputs.
+5e-6 absolute (the 2D SSIM map's bar), those of the downscaled octaves within
+1e-5.  The kernels shift each window's values by one value per 11-row band and
+8-column group, exact in real arithmetic, and take cs as 1 - D / (sigma11 +
+sigma22 + C2) with D from the blurred squared difference of the two images,
+which carries no rounding of their common level.  Measured at most 5.1e-6 at
+the downscaled octaves of the 1080p blob render, 2.5e-6 at octave 0.  Bands lie
+on one 11-row grid per image, so the values do not depend on the launch plan.
+The GPU downscales in float32, the oracle in double from the same float32
+inputs.
 """
 import numpy as np
 import pytest
@@ -23,8 +20,8 @@ from workloads import make_inputs, uniform_pair
 pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
-MAP_TOL = 2e-5           # octave 0
-OCTAVE_MAP_TOL = 2e-4    # octaves 1, 2, ... (downscaled: smaller features)
+MAP_TOL = 5e-6           # octave 0
+OCTAVE_MAP_TOL = 1e-5    # octaves 1, 2, ... (downscaled: smaller features)
 
 
 @pytest.fixture(scope="module")

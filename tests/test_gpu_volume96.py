@@ -10,7 +10,7 @@ every output voxel and every input gradient is compared:
   - per_image=True: the per-image means;
   - train=False (no saved fields, the backward recomputes);
   - the map of the C-ABI forward (ssim3d_fwd) element by element.
-The bars are the 3D parity bars: means 1e-5, maps 2e-4, gradients 1e-4 of the
+The bars are the 3D parity bars: means 1e-5, maps 3e-5, gradients 1e-4 of the
 largest oracle gradient.
 """
 import numpy as np
@@ -21,7 +21,7 @@ from workloads import noisy_copy, trilinear_noise_volume
 pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
-MAP_TOL_3D = 2e-4
+MAP_TOL_3D = 3e-5
 GRAD_RTOL = 1e-4
 SHAPE = (2, 3, 96, 96, 96)
 

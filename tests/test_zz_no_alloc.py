@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 MEAN_TOL = 1e-5
 GRAD_RTOL = 1e-4
-MAP_TOL = 2e-5
+MAP_TOL = 5e-6
 ETOOLARGE = -6
 
 
