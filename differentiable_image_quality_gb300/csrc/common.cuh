@@ -220,10 +220,12 @@ __device__ __forceinline__ float2 ssim_factors(const Moments &m, float2 sh)
     return make_float2(t.A1 * rcp_approx(t.B1), fmaf(-t.D, rcp_approx(t.B2), 1.0f));
 }
 
+// S = A1 (B2 - D) / (B1 B2): one reciprocal.  B2 - D is the numerator of cs,
+// so B2's rounding still reaches S only through D / B2.
 __device__ __forceinline__ float ssim_value(const Moments &m, float2 sh)
 {
-    const float2 lc = ssim_factors(m, sh);
-    return lc.x * lc.y;
+    const SsimTerms t = ssim_terms(m, sh);
+    return (t.A1 * (t.B2 - t.D)) * rcp_approx(t.B1 * t.B2);
 }
 
 // S and its derivatives with respect to the shifted moments:
