@@ -6,7 +6,8 @@ latency-critical caller that must not call cudaMalloc.  Instead of a caller's
 workspace it uses a fixed scratch array that the library keeps on each device.
 These checks call it through the C ABI (ctypes, raw device pointers) twice in a
 row, on two different problems, and compare each result with ssim_fwd's, within
-the bars the parity tests use.  The file is named to be collected last.
+the bars the parity tests use; one problem per padding is also compared with
+the oracle directly.  The file is named to be collected last.
 """
 import numpy as np
 import pytest
@@ -128,3 +129,22 @@ def test_noalloc_forward_rejects_problems_beyond_its_scratch(env):
     st = lib.ssim_fwd_noalloc(None, None, 64, 3, 1080, 1920, 0, None, None, None, 0, 0, None)
     assert st == ETOOLARGE
     assert b"ssim_fwd_noalloc" in lib.gbssim_strerror(st)
+
+
+@pytest.mark.parametrize("padding", ["valid", "same"])
+def test_noalloc_forward_matches_the_oracle(env, oracle_mod, padding):
+    """The no-allocation forward against the oracle directly: per-image means,
+    the map, and the saved fields, which are the gradients of each image's mean
+    with respect to both images (dLoss/dmean = 1)."""
+    torch, lib, dev = env
+    x, y = uniform_pair((2, 3, 57, 141), 904, std=0.1)
+    mean, smap, saved = _call(torch, lib, dev, _case(torch, dev, x, y, padding, True, True),
+                              noalloc=True)
+    torch.cuda.synchronize()
+    ref_mean, ref_map = oracle_mod.ssim2d(x, y, padding, want_map=True)
+    g1, g2 = oracle_mod.ssim2d_grad(x, y, np.ones(x.shape[0]), padding)
+    assert np.max(np.abs(mean.cpu().numpy() - ref_mean)) <= MEAN_TOL
+    assert np.max(np.abs(smap.cpu().numpy().astype(np.float64) - ref_map)) <= MAP_TOL
+    fields = saved.cpu().numpy().astype(np.float64).reshape((2,) + x.shape)
+    for got, ref in ((fields[0], g1), (fields[1], g2)):
+        assert np.max(np.abs(got - ref)) <= GRAD_RTOL * np.max(np.abs(ref))
