@@ -525,3 +525,18 @@ def test_flat_backgrounds(dev, oracle_mod, shape, padding, path):
     got = _run(dev, x, y, dl, padding, want_grad2, path, want_map=True)
     ref = _oracle(oracle_mod, x, y, dl, padding, want_grad2, want_map=True)
     _assert_parity(got, ref, want_grad2, f"{shape} {padding} {path}")
+
+
+@pytest.mark.parametrize("path", ["saved", "recompute"])
+@pytest.mark.parametrize("shape,padding", [((40, 3, 20, 24), "valid"), ((40, 3, 20, 24), "same"),
+                                           ((12, 2, 12, 13, 14), "valid"), ((12, 2, 12, 13, 14), "same")])
+def test_many_small_images(dev, oracle_mod, shape, padding, path):
+    """A batch of many small images (120 planes in 2D, 24 in 3D): more planes
+    than one wave of blocks holds, a per-image mean over blocks of many planes,
+    per-image upstream gradients."""
+    x, y = uniform_pair(shape, 4100 + len(shape), std=0.1)
+    dl = np.linspace(-1.0, 0.5, shape[0])
+    want_grad2 = padding == "same"
+    got = _run(dev, x, y, dl, padding, want_grad2, path, want_map=True)
+    ref = _oracle(oracle_mod, x, y, dl, padding, want_grad2, want_map=True)
+    _assert_parity(got, ref, want_grad2, f"{shape} {padding} {path}")
