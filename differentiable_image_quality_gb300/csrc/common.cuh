@@ -182,13 +182,19 @@ struct Moments {
     float m1, m2, es, ed;
 };
 
-// Upstream gradients of S with respect to the shifted moments (m1, m2, es, ed).
-// Because sigma11 and sigma22 enter S only as their sum, dS/dE[x'^2] and
-// dS/dE[y'^2] are one value, g_es.  In a flat window g_ed is of order 1 / C2
-// and g_es small; the chain rule meets g_ed only through x - y (see the
-// backward passes).
+// Upstream gradients of S for the backward.  g_es and g_ed are the derivatives
+// with respect to the shifted moments es and ed (because sigma11 and sigma22
+// enter S only as their sum, dS/dE[x'^2] and dS/dE[y'^2] are one value, g_es).
+// g_f1 and g_f2 are the first-moment maps of the chain rule with the window's
+// shift (s, t) folded in, so that every pixel takes the same form
+//   grad1 = B^T g_f1 + 2 (x - 1/2) B^T g_es + 2 (x - y) B^T g_ed:
+//   g_f1 = dS/dm1 + 2 (1/2 - s) g_es - 2 (s - t) g_ed
+//        = 2 cs (mu2 - mu1 l) / B1 + (1 - 2 mu1) g_es - 2 (mu1 - mu2) g_ed
+// (the shift cancels; g_f2 likewise with the images swapped).  In a flat
+// window g_ed is of order 1 / C2 and g_es small; g_ed meets only differences
+// of the two images.
 struct MomentGrads {
-    float g_m1, g_m2, g_es, g_ed;
+    float g_f1, g_f2, g_es, g_ed;
 };
 
 // S = l * cs with
@@ -228,12 +234,12 @@ __device__ __forceinline__ float ssim_value(const Moments &m, float2 sh)
     return (t.A1 * (t.B2 - t.D)) * rcp_approx(t.B1 * t.B2);
 }
 
-// S and its derivatives with respect to the shifted moments:
+// S and its derivatives:
 //   dS/des = l D / B2^2,   dS/ded = -l / B2,
 //   dS/dmu1 (sigma_sum and D fixed) = 2 cs (mu2 - mu1 l) / B1,
 // and through sigma_sum = es - m1^2 - m2^2, D = ed - (m1 - m2)^2:
 //   dS/dm1 = 2 cs (mu2 - mu1 l) / B1 - 2 m1 dS/des - 2 (m1 - m2) dS/ded,
-//   dS/dm2 = 2 cs (mu1 - mu2 l) / B1 - 2 m2 dS/des + 2 (m1 - m2) dS/ded.
+// which with the fold of MomentGrads gives g_f1 (g_f2 likewise).
 // When `valid` is false every derivative (and S) comes out as exactly zero:
 // l is zeroed before it is used.
 template <bool WANT_G2>
@@ -250,9 +256,10 @@ __device__ __forceinline__ float ssim_and_grads(const Moments &m, float2 sh, boo
     g.g_ed = -lr2;
     g.g_es = lr2 * Dr2;
     const float cr1x2 = valid ? cs * (r1 + r1) : 0.0f;
-    const float dm2 = (m.m1 - m.m2) * 2.0f;
-    g.g_m1 = fmaf(cr1x2, fmaf(-t.mu1, l, t.mu2), fmaf(-2.0f * m.m1, g.g_es, -dm2 * g.g_ed));
-    if (WANT_G2) g.g_m2 = fmaf(cr1x2, fmaf(-t.mu2, l, t.mu1), fmaf(-2.0f * m.m2, g.g_es, dm2 * g.g_ed));
+    const float du2 = 2.0f * (t.mu1 - t.mu2);
+    g.g_f1 = fmaf(cr1x2, fmaf(-t.mu1, l, t.mu2), fmaf(fmaf(-2.0f, t.mu1, 1.0f), g.g_es, -du2 * g.g_ed));
+    if (WANT_G2)
+        g.g_f2 = fmaf(cr1x2, fmaf(-t.mu2, l, t.mu1), fmaf(fmaf(-2.0f, t.mu2, 1.0f), g.g_es, du2 * g.g_ed));
     return S;
 }
 

@@ -10,7 +10,7 @@
 //             grad1 = B^T g_mu1 + 2 x B^T g_e + y B^T g_e12 (grad2 likewise),
 //             evaluated here with the derivatives of S with respect to
 //             es = E[x^2] + E[y^2] and ed = E[(x - y)^2] (E[xy] = (es - ed) / 2):
-//             grad1 = B^T g~_m1 + 2 (x - 1/2) B^T g_es + 2 (x - y) B^T g_ed.
+//             grad1 = B^T g_f1 + 2 (x - 1/2) B^T g_es + 2 (x - y) B^T g_ed.
 //
 // Design.  A CTA owns a vertical strip of columns of one (n, c) plane and walks
 // down a segment of its rows, 11 rows per step.  Per step:
@@ -105,8 +105,8 @@ __device__ __forceinline__ int stat_shift(int off) { return (4 - (off & 3)) & 3;
 //   xs, ys  [NBUF][XB] float               input rows: STEP rows of IWP floats
 //   hb      [HBUF] float4                  row-blurred statistics (m1, m2, es, ed)
 // gradient mode only:
-//   va      [STEP][P2] float2              adjoint column sums (g_m1, g_es)
-//   vb2     [STEP][P2] float2              (g_ed, g_m2)         [grad2]
+//   va      [STEP][P2] float2              adjoint column sums (g_f1, g_es)
+//   vb2     [STEP][P2] float2              (g_ed, g_f2)         [grad2]
 //   vc      [STEP][P1] float               g_ed                 [grad1 only]
 //   cbx,cby [CBB] float                    input pixels of this step's gradient rows,
 //                                          STEP rows of CBP floats
@@ -439,8 +439,8 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         const int g = item / STEP, k = item - g * STEP;
         const int q = R0 + (a_step * STEP) + k - 10;
         if (q < q0 || q >= q1) return;
-        float2 accA[KA];             // (B^T g_m1, B^T g_es)
-        float2 accB[KA];             // (B^T g_ed, B^T g_m2)    [G2]
+        float2 accA[KA];             // (B^T g_f1, B^T g_es)
+        float2 accB[KA];             // (B^T g_ed, B^T g_f2)    [G2]
         float accC[KA];              // B^T g_ed               [grad1 only]
         const float2 *pa = va + k * P2 + g * KA;   // 16-byte aligned (g * KA even)
 #pragma unroll
@@ -495,9 +495,9 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         // chain rule with the prefetched pixels (cb columns jj + CBOFF: 8-byte
         // aligned).  Per window p (shift (s, t)) and pixel r the term is
         //   g_m1 + 2 (x - s) g_es + 2 ((x - s) - (y - t)) g_ed
-        //     = g~_m1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed,
-        // g~_m1 being formed by the column pass, so the pixels here need no
-        // shift.  In a flat window g_ed is of order 1 / C2 and meets x - y,
+        //     = g_f1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed,
+        // g_f1 being formed with the derivatives (MomentGrads), so the pixels
+        // here need no shift.  In a flat window g_ed is of order 1 / C2 and meets x - y,
         // small where the two images agree; g_es is small there.
         const float *px = cbx + k * CBP + CBOFF + g * KA;
         const float *py = cby + k * CBP + CBOFF + g * KA;
@@ -542,8 +542,8 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
     };
     // ---- column pass state: registers of thread tid (statistic column sc0 + tid)
     float2 hA[STEP], hB[STEP];   // row-blurred (m1, m2), (es, ed)
-    float2 gA[STEP];             // (g_m1, g_es)
-    float2 gB[STEP];             // (g_ed, g_m2)    [G2]
+    float2 gA[STEP];             // (g_f1, g_es)
+    float2 gB[STEP];             // (g_ed, g_f2)    [G2]
     float gC[STEP];              // g_ed            [grad1 only]
 #pragma unroll
     for (int k = 0; k < STEP; ++k) {
@@ -649,19 +649,11 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
         if (GRAD) {
             MomentGrads gg;
             const float S = ssim_and_grads<G2>(mo, sh, ok, gg);
-            // fold the window's shift into the first map (see the chain rule in
-            // the adjoint row pass):
-            //   g~_m1 = g_m1 + 2 (1/2 - s) g_es - 2 (s - t) g_ed
-            //   g~_m2 = g_m2 + 2 (1/2 - t) g_es + 2 (s - t) g_ed
-            const float dst2 = 2.0f * (sh.x - sh.y);
-            const float g1 = fmaf(1.0f - 2.0f * sh.x, gg.g_es, fmaf(-dst2, gg.g_ed, gg.g_m1));
-            gA[k] = f2(g1, gg.g_es);
-            if (G2) {
-                const float g2 = fmaf(1.0f - 2.0f * sh.y, gg.g_es, fmaf(dst2, gg.g_ed, gg.g_m2));
-                gB[k] = f2(gg.g_ed, g2);
-            } else {
-                gC[k] = gg.g_ed;
-            }
+            // the first maps come with the window's shift folded in (see
+            // MomentGrads and the chain rule in the adjoint row pass)
+            gA[k] = f2(gg.g_f1, gg.g_es);
+            if (G2) gB[k] = f2(gg.g_ed, gg.g_f2);
+            else gC[k] = gg.g_ed;
             const bool own = ok && col_own && (k >= kown);
             if (want_mean) {
                 ssum += own ? S : 0.0f;
@@ -676,11 +668,11 @@ __device__ __forceinline__ void stream_body(const Ssim2dArgs &a, int block)
                 const float s12 = fmaf(-mo.m1, mo.m2, 0.5f * (mo.es - mo.ed));
                 reinterpret_cast<float4 *>(a.dump_stats)[o] =
                     make_float4(mo.m1 + sh.x, mo.m2 + sh.y, ss, s12);
-                const float dst2 = 2.0f * (sh.x - sh.y);
-                const float dmu1 = fmaf(-2.0f * sh.x, gg.g_es, fmaf(-dst2, gg.g_ed, gg.g_m1));
-                const float dmu2 = fmaf(-2.0f * sh.y, gg.g_es, fmaf(dst2, gg.g_ed, gg.g_m2));
+                // dS/dmu1 = g_f1 - g_es: the chain rule's per-pixel form
+                // g_f1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed against the textbook
+                // dS/dmu1 + 2 x dS/dE[x^2] + y dS/dE[xy]
                 reinterpret_cast<float4 *>(a.dump_grads)[o] =
-                    make_float4(dmu1, dmu2, gg.g_es + gg.g_ed, -2.0f * gg.g_ed);
+                    make_float4(gg.g_f1 - gg.g_es, gg.g_f2 - gg.g_es, gg.g_es + gg.g_ed, -2.0f * gg.g_ed);
             }
             va[k * P2 + tid] = ring_sum2<k>(gA);
             if (G2) vb2[k * P2 + tid] = ring_sum2<k>(gB);

@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
     float *mapc = a.map ? a.map + (size_t(plane) * a.Do) * cols + (col_ok ? c : 0) : nullptr;
 
     float2 PA[kTaps - 1], PB[kTaps - 1];  // pending Z sums of (m1, m2), (es, ed)
-    float2 QA[kTaps - 1], QB[kTaps - 1];  // adjoint: of (g_m1, g_es), (g_ed, g_m2)
+    float2 QA[kTaps - 1], QB[kTaps - 1];  // adjoint: of (g_f1, g_es), (g_ed, g_f2)
     float QC[kTaps - 1];                  // adjoint: of g_ed alone without grad_img2
 #pragma unroll
     for (int k = 0; k < kTaps - 1; ++k) {
@@ -479,10 +479,10 @@ __global__ void __launch_bounds__(kZThreads) ssim3d_z_kernel(const __grid_consta
         if (GRAD) {
             MomentGrads g;
             S = ssim_and_grads<G2>(mo, make_float2(kShift, kShift), true, g);
-            const float2 vA = zshift2(QA, f2(g.g_m1, g.g_es));
+            const float2 vA = zshift2(QA, f2(g.g_f1, g.g_es));
             float2 vB = f2(0.f, 0.f);
             float v12 = 0.f;
-            if (G2) vB = zshift2(QB, f2(g.g_ed, g.g_m2));
+            if (G2) vB = zshift2(QB, f2(g.g_ed, g.g_f2));
             else v12 = zshift1(QC, g.g_ed);
             emit(p, vA, vB, v12);
         } else {
@@ -650,9 +650,9 @@ __global__ void __launch_bounds__(GA::NT, 3) ssim3d_adjoint_kernel(const __grid_
     const size_t gbase = plane_off + size_t(col_ok ? qy : 0) * a.W + qx;
     const size_t gstride = size_t(a.H) * a.W;
 
-    // chain rule of slice s from (B^T g_m1, B^T g_es, B^T g_ed, B^T g_m2) at this
+    // chain rule of slice s from (B^T g_f1, B^T g_es, B^T g_ed, B^T g_f2) at this
     // pixel: per window (shift 1/2 for both images),
-    //   g_m1 + 2 x' g_es + 2 (x' - y') g_ed = g_m1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed;
+    //   g_m1 + 2 x' g_es + 2 (x' - y') g_ed = g_f1 + 2 (x - 1/2) g_es + 2 (x - y) g_ed;
     // in a flat window g_ed is of order 1 / C2 and meets x - y
     auto chain_step = [&](int s) {
         if (!col_ok) return;

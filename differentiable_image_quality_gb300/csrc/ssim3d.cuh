@@ -38,7 +38,7 @@ struct Ssim3dArgs {
     int tiles_x, tiles_y, zsegs, zseg_len;
     int col_blocks;            // z kernel: blocks of kZThreads columns per plane
     float4 *tfield;            // [planes, D, Ho, Wo] XY-blurred (m1, m2, es, ed)
-    float4 *ufield;            // [planes, D, Ho, Wo] Z-adjoint of (g_m1, g_es, g_ed, g_m2)
+    float4 *ufield;            // [planes, D, Ho, Wo] Z-adjoint of (g_f1, g_es, g_ed, g_f2)
     float *out1, *out2;        // adjoint: gradients or saved fields
     const float *dL;           // [N] or null (dL = 1)
     float inv_count;           // 1 / (C * Do * Ho * Wo)
